@@ -1,0 +1,415 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each check below is fixed by the method's text or by mathematics, not by the
+oracle: a hand-derived worked example, closed forms, special cases that reduce
+to a textbook or library routine, brute force on tiny inputs, and invariants.
+The mutation tests at the end plant plausible mistakes into the oracle (on the
+CPU) and confirm that at least one pin catches each.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.statekv_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+class _Cfg:
+    def __init__(self, **kw):
+        self.streams, self.layers = 1, 1
+        self.rope_alpha, self.rope_orig_ctx = 1.0, 0
+        self.rope_theta = 1e4
+        self.dtype = "f32"
+        self.__dict__.update(kw)
+
+
+# ----------------------------------------------------------------- pin checks
+def check_golden_zero_keys(o=orc):
+    """Worked example with all-zero keys: uniform attention over the visible
+    keys, so P, O, s and the selection are rationals derived by hand."""
+    g = _load("zero_keys_T2_B1.json")
+    st = g["setup"]
+    omega, ms = o.rope_frequencies(2, 1e4)
+    scale = o.logit_scale(2, ms)
+    # frame 0 always runs at B = 1; frame 1 at B = 1 and, separately, B = 2
+    for budget1, key in ((1, "kept_positions"), (2, "kept_positions_if_B2")):
+        state = o.UnitState(2)
+        for n, budget in ((0, 1), (1, budget1)):
+            q = np.array(st["q"][n], np.float64)
+            k = np.zeros((2, 2))
+            v = np.array(st["v"][n], np.float64)
+            O, info = o.prefill_unit_frame(state, q, k, v, n, budget=budget,
+                                           omega=omega, scale=scale, dtype="f32")
+            exp = g[f"frame{n}"]
+            np.testing.assert_array_equal(info["pool_pos"], exp["pool_positions"])
+            np.testing.assert_allclose(info["P"][0], exp["P"], atol=1e-15)
+            np.testing.assert_allclose(O[0], exp["O"], atol=1e-15)
+            np.testing.assert_allclose(info["scores"], exp["scores"], atol=1e-15)
+            want = exp[key] if n == 1 else exp["kept_positions"]
+            np.testing.assert_array_equal(state.comp_pos, want)
+        assert state.detailed_k.shape[0] == g["detailed_rows_after"]
+        np.testing.assert_array_equal(state.detailed_v, np.concatenate(st["v"]))
+
+
+def _complex_rope(x, positions, theta):
+    """Textbook RoPE written with complex numbers: the pair (x_k, x_{k+d/2}) is
+    the complex number x_k + i x_{k+d/2}, multiplied by exp(i p theta^(-2k/d))."""
+    x = np.asarray(x, np.float64)
+    assert x.ndim == 2
+    d = x.shape[-1]
+    half = d // 2
+    out = np.empty_like(x)
+    for t, p in enumerate(positions):
+        for k in range(half):
+            w = theta ** (-2.0 * k / d)
+            z = complex(x[t, k], x[t, k + half])
+            r = z * complex(math.cos(p * w), math.sin(p * w))
+            out[t, k], out[t, k + half] = r.real, r.imag
+    return out
+
+
+def check_rope_complex(o=orc):
+    rng = np.random.default_rng(1)
+    for d, theta in ((8, 1e4), (16, 1e6)):
+        x = rng.standard_normal((5, d))
+        pos = np.array([0, 1, 7, 1000, 131071])
+        omega, ms = o.rope_frequencies(d, theta)
+        assert ms == 1.0
+        got = o.rope_rotate(x, pos, omega)
+        want = _complex_rope(x, pos, theta)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-9)
+
+
+def _brute_full_causal(qs, ks, vs, theta, scale, G):
+    """Ordinary causal self-attention over the whole token sequence, one query
+    at a time, with float32-stored rotated q/k (loops; tiny inputs only).
+    qs: [NT, Hq=G, d], ks/vs: [NT, d] (one KV head)."""
+    NT, _, d = qs.shape
+    pos = np.arange(NT)
+    qr = np.stack([_complex_rope(qs[:, g, :], pos, theta) for g in range(G)], 1)
+    kr = _complex_rope(ks, pos, theta)
+    qr = qr.astype(np.float32).astype(np.float64)
+    kr = kr.astype(np.float32).astype(np.float64)
+    out = np.zeros_like(qs)
+    for t in range(NT):
+        for g in range(G):
+            logits = [float(np.dot(qr[t, g], kr[j])) * scale for j in range(t + 1)]
+            mx = max(logits)
+            w = [math.exp(a - mx) for a in logits]
+            tot = sum(w)
+            out[t, g] = sum(w[j] / tot * vs[j] for j in range(t + 1))
+    return out
+
+
+def check_full_sa_when_budget_covers_all(o=orc):
+    """With B >= N*T nothing is ever evicted, so every frame's output must be
+    exactly full causal self-attention over the whole stream (Full SA)."""
+    G, T, d, N = 2, 4, 8, 3
+    theta = 1e4
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((N, G, T, d))
+    k = rng.standard_normal((N, T, d))
+    v = rng.standard_normal((N, T, d))
+    omega, ms = o.rope_frequencies(d, theta)
+    scale = o.logit_scale(d, ms)
+    state = o.UnitState(d)
+    outs = []
+    for n in range(N):
+        O, _ = o.prefill_unit_frame(state, q[n], k[n], v[n], n, budget=N * T,
+                                    omega=omega, scale=scale, dtype="f32")
+        outs.append(O.transpose(1, 0, 2))          # [T, G, d]
+    got = np.concatenate(outs)
+    # textbook softmax scale 1/sqrt(d) (alpha = 1)
+    want = _brute_full_causal(q.transpose(0, 2, 1, 3).reshape(N * T, G, d),
+                              k.reshape(N * T, d), v.reshape(N * T, d),
+                              theta, 1.0 / math.sqrt(d), G)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def check_zero_budget_is_per_frame_causal(o=orc):
+    """B = 0: no cross-frame state, so each frame is plain causal attention
+    over its own tokens -- torch's scaled_dot_product_attention in fp64."""
+    G, T, d = 3, 6, 16
+    theta = 1e6
+    rng = np.random.default_rng(3)
+    omega, ms = o.rope_frequencies(d, theta)
+    scale = o.logit_scale(d, ms)
+    state = o.UnitState(d)
+    for n in range(3):
+        q = rng.standard_normal((G, T, d))
+        k = rng.standard_normal((T, d))
+        v = rng.standard_normal((T, d))
+        O, _ = o.prefill_unit_frame(state, q, k, v, n, budget=0, omega=omega,
+                                    scale=scale, dtype="f32")
+        pos = n * T + np.arange(T)
+        qr = np.stack([_complex_rope(q[g], pos, theta) for g in range(G)])
+        kr = _complex_rope(k, pos, theta)
+        qr = torch.from_numpy(qr.astype(np.float32).astype(np.float64))
+        kr = torch.from_numpy(kr.astype(np.float32).astype(np.float64))
+        vt = torch.from_numpy(v)
+        want = torch.nn.functional.scaled_dot_product_attention(
+            qr[None], kr[None, None].expand(1, G, T, d),
+            vt[None, None].expand(1, G, T, d), is_causal=True,
+            scale=1.0 / math.sqrt(d))[0]
+        np.testing.assert_allclose(O, want.numpy(), rtol=0, atol=1e-12)
+        assert state.comp_k.shape[0] == 0
+
+
+def check_topb_rank_definition(o=orc):
+    """Top-B against the rank definition: j is kept iff fewer than B
+    candidates beat it (higher score, or equal score at a lower position)."""
+    rng = np.random.default_rng(11)
+    for trial in range(30):
+        m = int(rng.integers(1, 40))
+        B = int(rng.integers(0, 45))
+        s = rng.integers(0, 6, size=m).astype(np.float64) / 5.0   # many ties
+        pos = rng.permutation(1000)[:m]
+        keep = o.select_top_b(s, pos, B)
+        want = [j for j in range(m)
+                if sum((s[i] > s[j]) or (s[i] == s[j] and pos[i] < pos[j])
+                       for i in range(m)) < B]
+        assert sorted(keep.tolist()) == sorted(want)
+        assert list(pos[keep]) == sorted(pos[keep])
+
+
+# ----------------------------------------------------------------- the tests
+def test_golden_zero_keys():
+    check_golden_zero_keys()
+
+
+def test_rope_is_complex_rotation():
+    check_rope_complex()
+
+
+def test_full_sa_special_case():
+    check_full_sa_when_budget_covers_all()
+
+
+def test_zero_budget_matches_sdpa():
+    check_zero_budget_is_per_frame_causal()
+
+
+def test_topb_rank_definition():
+    check_topb_rank_definition()
+
+
+def test_yarn_golden_and_limits():
+    g = _load("yarn_d4.json")
+    om, ms = orc.rope_frequencies(g["head_dim"], g["theta"], g["alpha"], g["orig_ctx"])
+    np.testing.assert_allclose(om, g["omega"], atol=g["abs_tol"])
+    assert abs(ms - g["mscale"]) < g["abs_tol"]
+    # alpha == 1 is plain RoPE whatever L_orig says
+    plain, m1 = orc.rope_frequencies(128, 1e6)
+    same, m2 = orc.rope_frequencies(128, 1e6, 1.0, 32960)
+    np.testing.assert_array_equal(plain, same)
+    assert m1 == m2 == 1.0
+    # very high frequencies (many turns inside L_orig) are left alone; the
+    # lowest frequencies are interpolated by exactly 1/alpha
+    om4, _ = orc.rope_frequencies(128, 1e6, 4.0, 32960)
+    wl = 2 * math.pi / plain
+    hi = 32960 / wl > 32
+    lo = 32960 / wl < 1
+    assert hi.any() and lo.any()
+    np.testing.assert_array_equal(om4[hi], plain[hi])
+    np.testing.assert_allclose(om4[lo], plain[lo] / 4.0, rtol=1e-15)
+    assert np.all(np.diff(om4) < 0)            # still strictly decreasing
+    assert np.all(om4 <= plain) and np.all(om4 >= plain / 4.0)
+
+
+def test_rope_norm_and_relative_position():
+    rng = np.random.default_rng(5)
+    d = 64
+    omega, _ = orc.rope_frequencies(d, 1e6, 4.0, 32960)
+    x = rng.standard_normal((7, d))
+    y = rng.standard_normal((7, d))
+    p = np.arange(7) * 911 + 3
+    xr = orc.rope_rotate(x, p, omega)
+    # per-pair norms are preserved by a rotation
+    h = d // 2
+    np.testing.assert_allclose(xr[:, :h] ** 2 + xr[:, h:] ** 2,
+                               x[:, :h] ** 2 + x[:, h:] ** 2, rtol=1e-12)
+    # q'(p)·k'(p') depends only on p - p' (the property virtual positions keep)
+    for delta in (1, 4096, 131072):
+        a = orc.rope_rotate(x, p, omega) @ orc.rope_rotate(y, p[::-1], omega).T
+        b = orc.rope_rotate(x, p + delta, omega) @ orc.rope_rotate(y, p[::-1] + delta, omega).T
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-9 * np.abs(a).max())
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(2)
+    x32 = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                          (rng.standard_normal(2000) * 1e-30).astype(np.float32),
+                          np.array([0.0, -0.0, 1.0, 3.0], np.float32)])
+    # include exact midpoints between neighbouring bf16 values (ties to even)
+    mids = (torch.arange(1, 200, dtype=torch.int32) << 16) | (1 << 15)
+    x32 = np.concatenate([x32, mids.view(torch.float32).numpy()])
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(orc.bf16_round(x32.astype(np.float64)), want)
+
+
+def test_scores_are_a_distribution():
+    rng = np.random.default_rng(9)
+    G, T, d, c = 3, 10, 16, 17
+    q = rng.standard_normal((G, T, d))
+    K = rng.standard_normal((c + T, d))
+    V = rng.standard_normal((c + T, d))
+    O, P = orc.attend_frame(q, K, V, c, 0.3)
+    np.testing.assert_allclose(P.sum(-1), 1.0, atol=1e-14)
+    s = orc.importance_scores(P)
+    assert np.all(s >= 0)
+    assert abs(s.sum() - 1.0) < 1e-14
+    # masked entries are exactly zero; O is a convex combination of V rows
+    for i in range(T):
+        assert np.all(P[:, i, c + i + 1:] == 0)
+    assert np.all(O <= V.max(0) + 1e-12) and np.all(O >= V.min(0) - 1e-12)
+
+
+def test_gqa_duplicate_heads_and_single_head():
+    rng = np.random.default_rng(4)
+    T, d, c = 8, 16, 5
+    q1 = rng.standard_normal((1, T, d))
+    K = rng.standard_normal((c + T, d))
+    V = rng.standard_normal((c + T, d))
+    O1, P1 = orc.attend_frame(q1, K, V, c, 0.25)
+    O2, P2 = orc.attend_frame(np.concatenate([q1, q1]), K, V, c, 0.25)
+    np.testing.assert_array_equal(O2[0], O1[0])
+    np.testing.assert_array_equal(O2[1], O1[0])
+    np.testing.assert_allclose(orc.importance_scores(P2), orc.importance_scores(P1),
+                               rtol=1e-15)
+    # with one head, s_j is the plain mean over the T queries
+    np.testing.assert_allclose(orc.importance_scores(P1), P1[0].mean(0), rtol=1e-15)
+
+
+def test_state_invariants_over_a_stream():
+    cfg = _Cfg(q_heads=4, kv_heads=2, head_dim=16, frame_tokens=5, budget=12,
+               rope_theta=1e6, rope_alpha=4.0, rope_orig_ctx=40, dtype="bf16")
+    o = orc.StateKVOracle(cfg)
+    rng = np.random.default_rng(6)
+    for n in range(7):
+        q = rng.standard_normal((1, 1, 4, 5, 16))
+        k = rng.standard_normal((1, 1, 2, 5, 16))
+        v = orc.bf16_round(rng.standard_normal((1, 1, 2, 5, 16)))
+        o.prefill_frame(q, k, v)
+        for st in o.units.values():
+            c = st.comp_k.shape[0]
+            assert c == min(cfg.budget, (n + 1) * 5)
+            assert st.detailed_k.shape[0] == (n + 1) * 5
+            assert len(set(st.comp_pos.tolist())) == c
+            assert st.comp_pos.min() >= 0 and st.comp_pos.max() < (n + 1) * 5
+            # compressed rows are copies of detailed rows at the same position
+            np.testing.assert_array_equal(st.comp_k, st.detailed_k[st.comp_pos])
+            np.testing.assert_array_equal(st.comp_v, st.detailed_v[st.comp_pos])
+            # stored keys are storage-rounded
+            np.testing.assert_array_equal(st.detailed_k, orc.bf16_round(st.detailed_k))
+
+
+# -------------------------------------------------------- planted mistakes
+def _mut_mask_offbyone(monkeypatch):
+    real = orc.attend_frame
+
+    def bad(q_rot, pool_k, pool_v, n_compressed, scale):
+        # frame key i' visible iff i' < i  (drops the diagonal) -- emulate by
+        # shifting the compressed count so the diagonal is masked
+        q = np.asarray(q_rot, np.float64)
+        K = np.asarray(pool_k, np.float64)
+        V = np.asarray(pool_v, np.float64)
+        G, T, _ = q.shape
+        m = K.shape[0]
+        c = n_compressed
+        z = np.einsum("gtd,jd->gtj", q, K) * scale
+        i = np.arange(T)[:, None]
+        j = np.arange(m)[None, :]
+        vis = (j < c) | ((j - c) < i) | ((i == 0) & (j == c))
+        z = np.where(vis[None], z, -np.inf)
+        z = z - z.max(-1, keepdims=True)
+        e = np.where(vis[None], np.exp(z), 0.0)
+        P = e / e.sum(-1, keepdims=True)
+        return np.einsum("gtj,jd->gtd", P, V), P
+    monkeypatch.setattr(orc, "attend_frame", bad)
+    return real
+
+
+def _mut_score_visible_mean(monkeypatch):
+    def bad(P):
+        G, T, m = P.shape
+        flat = P.reshape(G * T, m)
+        cnt = np.maximum((flat > 0).sum(0), 1)
+        return flat.sum(0) / cnt
+    monkeypatch.setattr(orc, "importance_scores", bad)
+
+
+def _mut_tiebreak_high(monkeypatch):
+    def bad(scores, positions, budget):
+        s = np.asarray(scores, np.float64)
+        p = np.asarray(positions, np.int64)
+        if s.shape[0] <= budget:
+            keep = np.arange(s.shape[0])
+        else:
+            keep = np.lexsort((-p, -s))[:budget]
+        return keep[np.argsort(p[keep], kind="stable")]
+    monkeypatch.setattr(orc, "select_top_b", bad)
+
+
+def _mut_rope_sign(monkeypatch):
+    def bad(x, positions, omega):
+        x = np.asarray(x, np.float64)
+        h = x.shape[-1] // 2
+        ang = np.asarray(positions, np.float64)[:, None] * omega[None, :]
+        a, b = x[..., :h], x[..., h:]
+        return np.concatenate([a * np.cos(ang) + b * np.sin(ang),
+                               b * np.cos(ang) - a * np.sin(ang)], -1)
+    monkeypatch.setattr(orc, "rope_rotate", bad)
+
+
+def _mut_rope_freq_index(monkeypatch):
+    real = orc.rope_frequencies
+
+    def bad(head_dim, theta, alpha=1.0, orig_ctx=0):
+        om, ms = real(head_dim, theta, alpha, orig_ctx)
+        k = np.arange(head_dim // 2)
+        return np.power(float(theta), -1.0 * k / head_dim), ms   # 2k/d -> k/d
+    monkeypatch.setattr(orc, "rope_frequencies", bad)
+
+
+def _mut_no_scale(monkeypatch):
+    monkeypatch.setattr(orc, "logit_scale", lambda d, ms: 1.0)
+
+
+def _mut_pv_transposed_heads(monkeypatch):
+    real = orc.attend_frame
+
+    def bad(q_rot, pool_k, pool_v, n_compressed, scale):
+        O, P = real(q_rot, pool_k, pool_v, n_compressed, scale)
+        return O[::-1].copy(), P
+    monkeypatch.setattr(orc, "attend_frame", bad)
+
+
+_CHECKS = [check_golden_zero_keys, check_rope_complex,
+           check_full_sa_when_budget_covers_all,
+           check_zero_budget_is_per_frame_causal, check_topb_rank_definition]
+
+
+@pytest.mark.parametrize("mutation", [
+    _mut_mask_offbyone, _mut_score_visible_mean, _mut_tiebreak_high,
+    _mut_rope_sign, _mut_rope_freq_index, _mut_no_scale,
+    _mut_pv_transposed_heads])
+def test_planted_mistake_is_caught(monkeypatch, mutation):
+    mutation(monkeypatch)
+    caught = 0
+    for chk in _CHECKS:
+        try:
+            chk(orc)
+        except AssertionError:
+            caught += 1
+    assert caught >= 1, f"no pin caught {mutation.__name__}"
