@@ -1,0 +1,384 @@
+"""Benchmark: StateKV streaming prefill throughput on GB300.
+
+Metric: video frames/s through streaming prefill, all layers, B=4096, T=256,
+on the InternVL3-2B attention geometry (28 layers, 12 query / 2 KV heads,
+head_dim 128, 512 frames per video, static YaRN alpha=4), with the fraction
+of the bf16 tensor-core peak reached by the attention kernel.
+
+One step = one whole video: the handle is reset and all 512 frames stream
+through every layer (the fill phase included, exactly as a user runs it).
+Inputs: a ring of 16 distinct seeded synthetic frames resident in HBM, frame
+n uses ring slot n % 16; the per-frame working set (compressed state of all
+layers ~117 MB, Q/O ~44 MB, detailed-state append, scratch) exceeds L2.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+N > 1 runs under torchrun, one rank per GPU, each rank streaming its own
+video (independent streams; no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "video frames/sec through streaming prefill (all layers, B=4096,T=256); % bf16 TC peak"
+UNIT = "frames/s"
+WORKLOAD = "internvl3_2b_stack"
+RING = 16
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=j["hbm_gbs"], tc=j["bf16_tflops"], tc_sus=j["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sus=1700.0, src="fallback")
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        dist.init_process_group(backend)
+        return dist, int(os.environ["RANK"]), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f).get(kernel)
+    if not j:
+        return None
+    src = os.path.join(ROOT, "kv_cache_compression_frame_gb300", "csrc", j["source"])
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return j["bytes_per_launch"] if h == j["source_sha"] else None
+
+
+# --------------------------------------------------------------- CPU oracle
+def _oracle_frame_sample(sh, layers: int, seed: int = 1):
+    """Time the oracle on `layers` layers of one steady-state frame (the
+    compressed state full, c = B).  Returns seconds."""
+    import numpy as np
+    import oracle.statekv_oracle as orc
+    from synth import FrameSource
+    src = FrameSource(sh)
+    omega, ms = orc.rope_frequencies(sh.head_dim, sh.rope_theta, sh.rope_alpha, sh.rope_orig_ctx)
+    scale = orc.logit_scale(sh.head_dim, ms)
+    rng = np.random.default_rng(seed)
+    n = sh.budget // sh.frame_tokens            # first frame with a full state
+    G, B, d = sh.group, sh.budget, sh.head_dim
+    states = []
+    for _ in range(layers * sh.kv_heads):       # synthetic full state (not timed)
+        st = orc.UnitState(d)
+        pos = np.arange(B, dtype=np.int64)
+        st.comp_k = orc.round_to_storage(orc.rope_rotate(rng.standard_normal((B, d)), pos, omega), sh.dtype)
+        st.comp_v = orc.round_to_storage(rng.standard_normal((B, d)), sh.dtype)
+        st.comp_pos = pos
+        states.append(st)
+    inputs = [src.layer_frame(0, l, n) for l in range(layers)]
+    t0 = time.perf_counter()
+    i = 0
+    for l in range(layers):
+        q, k, v = inputs[l]
+        for hk in range(sh.kv_heads):
+            orc.prefill_unit_frame(states[i], q[hk * G:(hk + 1) * G], k[hk], v[hk], n,
+                                   budget=B, omega=omega, scale=scale, dtype=sh.dtype)
+            i += 1
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(sh, layers: int = 3) -> dict:
+    secs = _oracle_frame_sample(sh, layers)
+    per_frame = secs * sh.layers / layers
+    return {"value": 1.0 / per_frame, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"fp64 NumPy oracle, {layers} of {sh.layers} layers "
+                      f"({layers * sh.kv_heads} of {sh.units} units) of one steady-state "
+                      f"frame (c=B={sh.budget}), {secs:.1f} s, scaled x{sh.layers}/{layers}"}
+
+
+def run_reference(args, sh):
+    dist, rank, ws, _ = _dist()
+    if rank != 0:
+        return
+    layers = 1
+    for _ in range(args.warmup):
+        _oracle_frame_sample(sh, layers)
+    times = [_oracle_frame_sample(sh, layers, seed=2 + i) for i in range(args.steps)]
+    tot = sum(times) * sh.layers / layers
+    value = args.steps / tot
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": sh.layers, "q_heads": sh.q_heads,
+                   "kv_heads": sh.kv_heads, "head_dim": sh.head_dim, "T": sh.frame_tokens,
+                   "B": sh.budget, "step": "one steady-state frame, all layers (bounded "
+                                           "sample: 1 layer timed, scaled x28)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "one layer (2 units) of one steady-state frame per step, "
+                                   "scaled to all 28 layers"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- GPU
+def run_gpu(args, sh):
+    import torch
+    from kv_cache_compression_frame_gb300 import StateKV, StateKVConfig
+    from synth import FrameSource
+
+    dist, rank, ws, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = _peaks()
+    frames = args.frames or sh.frames
+    src = FrameSource(sh, seed=sh.seed + rank)
+    ring = [src.frame(i) for i in range(RING)]
+    dq = [torch.from_numpy(r[0]).to(torch.bfloat16).to(dev) for r in ring]
+    dk = [torch.from_numpy(r[1]).to(torch.bfloat16).to(dev) for r in ring]
+    dv = [torch.from_numpy(r[2]).to(torch.bfloat16).to(dev) for r in ring]
+    o = torch.empty_like(dq[0])
+    h = StateKV(StateKVConfig.from_shape(sh, max_frames=frames), device=local)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_video():
+        h.reset()
+        for n in range(frames):
+            r = n % RING
+            h.prefill_frame(dq[r], dk[r], dv[r], o, stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        one_video()
+    h.check_device_status()
+
+    # timed region: K whole videos, per-kernel events recorded on the stream
+    clocks = ClockSampler(local)
+    h.profile_enable(True)
+    torch.cuda.synchronize()
+    barrier()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        one_video()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    prof = h.profile_read()
+    h.profile_enable(False)
+    h.check_device_status()
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    total_frames = args.steps * frames * ws
+    value = total_frames / (ms / 1000.0)
+
+    # per-frame latency vs n (one extra, untimed video)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(frames + 1)]
+    h.reset()
+    evs[0].record(stream)
+    for n in range(frames):
+        r = n % RING
+        h.prefill_frame(dq[r], dk[r], dv[r], o, stream)
+        evs[n + 1].record(stream)
+    torch.cuda.synchronize()
+    per_frame = [evs[i].elapsed_time(evs[i + 1]) * 1000.0 for i in range(frames)]
+    n_full = sh.budget // sh.frame_tokens
+    steady = per_frame[n_full:]
+    q1 = len(steady) // 4
+    flat = (statistics.median(steady[-q1:]) / statistics.median(steady[:q1])) if q1 else None
+
+    # e2e: host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq = [torch.from_numpy(r[0]).to(torch.bfloat16).pin_memory() for r in ring]
+        hk = [torch.from_numpy(r[1]).to(torch.bfloat16).pin_memory() for r in ring]
+        hv = [torch.from_numpy(r[2]).to(torch.bfloat16).pin_memory() for r in ring]
+        ho = torch.empty(dq[0].shape, dtype=torch.bfloat16).pin_memory()
+
+        def one_video_host():
+            h.reset()
+            for n in range(frames):
+                r = n % RING
+                h.prefill_frame_host(hq[r], hk[r], hv[r], ho, stream)
+
+        one_video_host()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            one_video_host()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        in_b = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * 2 * frames
+        out_b = ho.numel() * 2 * frames
+        e2e = {"value": args.e2e_steps * frames * ws / (ems / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b,
+               "steps": args.e2e_steps}
+
+    # roofline of the dominant kernel (attention) over the timed region
+    flops_timed = args.steps * sum(sh.attention_flops(n) for n in range(frames))
+    attn_ms, attn_n = prof["attention"]
+    achieved = flops_timed / (attn_ms / 1000.0) / 1e12
+    step_flops = sum(sh.attention_flops(n) for n in range(frames))
+    q_bytes = sh.streams * sh.layers * sh.q_heads * sh.frame_tokens * sh.head_dim * 2
+    kv_bytes = sh.streams * sh.layers * sh.kv_heads * sh.frame_tokens * sh.head_dim * 2
+    rope_bytes = 2 * q_bytes + 6 * kv_bytes
+    kernels = {}
+    for name, (kms, cnt) in prof.items():
+        ent = {"launches": cnt, "ms_per_launch": kms / max(cnt, 1),
+               "share": kms / max(sum(x[0] for x in prof.values()), 1e-9)}
+        if name == "rope":
+            ent["gbs"] = rope_bytes / (kms / max(cnt, 1) / 1000.0) / 1e9
+            ent["algorithmic_bytes_per_launch"] = rope_bytes
+        kernels[name] = ent
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": sh.layers, "q_heads": sh.q_heads,
+                       "kv_heads": sh.kv_heads, "head_dim": sh.head_dim,
+                       "T": sh.frame_tokens, "B": sh.budget, "frames_per_step": frames,
+                       "rope_alpha": sh.rope_alpha, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2 (16-frame ring, 117 MB compressed state)"},
+            "tflops_algorithmic": step_flops * args.steps / (ms / 1000.0) / 1e12,
+            "tflops_executed": 1.5 * step_flops * args.steps / (ms / 1000.0) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tc_sus"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["tc_sus"],
+                         "traffic": _traffic("attention"),
+                         "kernel": "attn_tc_kernel<128>",
+                         "peak_kind": f"bf16 sustained ({peaks['src']})",
+                         "flops_per_launch_steady": sh.attention_flops(n_full),
+                         "ms_per_launch": attn_ms / max(attn_n, 1)},
+            "kernels": kernels,
+            "per_frame_us": {"fill_mean": statistics.mean(per_frame[:n_full]) if n_full else None,
+                             "steady_median": statistics.median(steady) if steady else None,
+                             "steady_p99": sorted(steady)[int(0.99 * (len(steady) - 1))] if steady else None,
+                             "last_quarter_over_first_quarter": flat},
+            "e2e": e2e,
+            "gpu_launches": sum(c for _, c in prof.values()),
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline and ws == 1:
+            line["cpu_baseline"] = cpu_baseline(sh)
+        print(json.dumps(line), flush=True)
+    h.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--frames", type=int, default=0, help="frames per video (default: N of the workload)")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from synth import SHAPES
+    sh = SHAPES[args.workload]
+    if args.impl == "reference":
+        run_reference(args, sh)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_gpu(args, sh)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * statekv.h -- C ABI of libstatekv, the GB300 (sm_103a) implementation of
+ * StateKV streaming video prefill.
+ *
+ * Method: "Linear Scaling Video VLMs for Long Video Understanding" (StateKV,
+ * ECCV 2026), papernotes.org summary, section 方法详解:
+ *   整体框架 (overall framework) -- frames arrive one at a time, T visual tokens
+ *     each; in every layer the frame attends only to a fixed-capacity
+ *     compressed state C_{n-1} and to itself, so the per-frame cost is
+ *     O(T^2 + BT) and the prefill is linear in the number of frames N;
+ *   关键设计 1 (dual state) -- per layer a detailed state D_n holding every
+ *     frame's K/V (kept for text decoding) and a compressed state C_n with
+ *     |K̄_n| = B; Q_n attends over [K̄_{n-1}; K_n];
+ *   关键设计 2 (temporal-sink update) -- candidate pool U_n = S̄_{n-1} ∪ {1..T},
+ *     score s_j = mean attention the frame's queries pay to key j,
+ *     S̄_n = TopK({s_j}, B) rebuilds C_n;
+ *   关键设计 3 (virtual length, static RoPE scale) -- RoPE angles use the
+ *     logical stream position L_n = nT (+ i); one global scale alpha is fixed
+ *     before prefill and never changes.
+ *
+ * Readings of points the page leaves open (fixed here, per KV head):
+ *   - mask: compressed keys fully visible; frame key i' visible to query i iff
+ *     i' <= i;
+ *   - s_j averages P over all G*T query rows of the G query heads that share
+ *     the KV head (a query that cannot see j contributes 0);
+ *   - Top-B ties go to the lower virtual position;
+ *   - positions p = position_offset + n*T + i, n 0-based;
+ *   - alpha != 1 is YaRN NTK-by-parts (beta_fast 32, beta_slow 1) with logit
+ *     factor mscale^2, mscale = 0.1 ln(alpha) + 1;
+ *   - C and D hold post-RoPE keys in the storage dtype.
+ *
+ * Threading and streams: a handle is not thread-safe; calls on one handle
+ * must be serialised by the caller.  All device work of a call is enqueued
+ * asynchronously on the caller's CUDA stream (cudaStream_t passed as void*,
+ * NULL = the legacy default stream); results are valid once that stream has
+ * reached the point after the call.
+ *
+ * Errors: every entry point returns an int status (STATEKV_OK or a negative
+ * STATEKV_E_*).  Nothing aborts and no C++ exception crosses the ABI.  Host
+ * argument checks happen before any device work, so a call rejected with
+ * E_INVALID_ARG / E_UNSUPPORTED / E_CAPACITY leaves the handle unchanged.
+ * E_CUDA means a CUDA call failed (the handle's device state is then
+ * unspecified; destroy it).  Device-side bounded waits that give up record a
+ * status that statekv_check_device_status() reports as E_TIMEOUT.
+ */
+#ifndef STATEKV_H_
+#define STATEKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define STATEKV_OK              0
+#define STATEKV_E_INVALID_ARG  -1   /* null pointer, bad size, bad index      */
+#define STATEKV_E_UNSUPPORTED  -2   /* valid but not implemented (e.g. d=96)  */
+#define STATEKV_E_CAPACITY     -3   /* detailed state full (n == max_frames)  */
+#define STATEKV_E_OOM          -4   /* device allocation failed at create     */
+#define STATEKV_E_CUDA         -5   /* a CUDA runtime/driver call failed      */
+#define STATEKV_E_TIMEOUT      -6   /* a device-side bounded wait gave up     */
+#define STATEKV_E_DEVICE       -7   /* a device-side consistency check failed */
+
+/* storage dtypes */
+#define STATEKV_BF16 0              /* bf16 storage, fp32 accumulation        */
+#define STATEKV_F32  1              /* fp32 storage and arithmetic            */
+
+/* kernels, for statekv_profile_read() */
+#define STATEKV_KERNEL_ROPE_TABLE 0 /* per-frame cos/sin table                */
+#define STATEKV_KERNEL_ROPE       1 /* RoPE at virtual positions + appends    */
+#define STATEKV_KERNEL_ATTENTION  2 /* two-sweep attention + key column sums  */
+#define STATEKV_KERNEL_SELECT     3 /* score finish, Top-B, slot-reuse gather */
+#define STATEKV_NUM_KERNELS       4
+
+typedef struct statekv_handle statekv_handle;   /* opaque */
+
+/*
+ * Configuration of one handle.  Every (stream, layer, KV head) is an
+ * independent unit with its own C and D; all units advance together, one
+ * frame per statekv_prefill_frame call.
+ *   num_streams   S >= 1   independent videos stepped together
+ *   num_layers    L >= 1   transformer layers (inputs per layer are given)
+ *   num_q_heads   Hq       query heads; Hq % Hkv == 0, G = Hq / Hkv
+ *   num_kv_heads  Hkv >= 1 KV heads (query head j uses KV head j / G)
+ *   head_dim      d        64 or 128
+ *   frame_tokens  T >= 1   visual tokens per frame
+ *   budget        B >= 0   compressed-state capacity (关键设计 1, |K̄| = B)
+ *   max_frames    N_max    capacity of the detailed state D, in frames
+ *   dtype         STATEKV_BF16 or STATEKV_F32
+ *   device        CUDA device ordinal the handle lives on
+ *   rope_theta    RoPE base theta (> 1)
+ *   rope_alpha    static global RoPE scale alpha >= 1, fixed for the
+ *                 handle's lifetime (关键设计 3)
+ *   rope_orig_ctx YaRN original context L_orig (> 0 when alpha != 1)
+ *   position_offset virtual position of the first video token (>= 0)
+ * Limits: G*T <= 65536 query rows per unit; B + T <= 28672; positions must
+ * fit in int32.
+ */
+typedef struct statekv_config {
+    int32_t num_streams;
+    int32_t num_layers;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t frame_tokens;
+    int32_t budget;
+    int32_t max_frames;
+    int32_t dtype;
+    int32_t device;
+    double  rope_theta;
+    double  rope_alpha;
+    int64_t rope_orig_ctx;
+    int64_t position_offset;
+} statekv_config;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* statekv_status_string(int status);
+
+/*
+ * Create a handle: validates cfg, allocates on cfg->device (current device is
+ * restored on return) the compressed pool [S][L][Hkv][B+T][d] for K and V,
+ * its positions [S][L][Hkv][B+T] int32, the detailed state
+ * [S][L][Hkv][N_max*T][d] for K and V, scratch (rotated queries, per-tile key
+ * column sums, scores) and one frame of staging for the host-buffer entry
+ * point.  All device memory is zero-filled.  The handle owns it all.
+ * On failure *out is set to NULL and nothing is leaked.
+ */
+int statekv_create(const statekv_config* cfg, statekv_handle** out);
+
+/* Free everything the handle owns (synchronises the device first). NULL ok. */
+int statekv_destroy(statekv_handle* h);
+
+/*
+ * One frame step n (= statekv_frame_index(h)) for every unit (整体框架,
+ * 关键设计 1-3):
+ *   1. rotate Q and K at p = position_offset + n*T + i with the static
+ *      frequencies, store K' and V into D rows [n*T, n*T+T) and into the
+ *      compressed pool after the c = min(B, n*T) live slots;
+ *   2. O = softmax(Q' [K̄_{n-1}; K'_n]^T * mscale^2/sqrt(d), masked) [V̄; V];
+ *   3. s_j for every pool slot, Top-B with ties to the lower position;
+ *   4. C_n keeps the B winners: evicted slots are refilled in place by the
+ *      surviving frame rows (slot order is not position order).
+ * Pointers are DEVICE pointers on the handle's device, caller-owned,
+ * contiguous, in the storage dtype:
+ *   q, o : [S][L][Hq][T][d]      (o is written, never read)
+ *   k, v : [S][L][Hkv][T][d]     (pre-RoPE keys; values)
+ * q/k/v must not alias o or handle memory.  Returns E_CAPACITY when
+ * n == max_frames.  On success the frame index advances by one.
+ */
+int statekv_prefill_frame(statekv_handle* h, const void* q, const void* k,
+                          const void* v, void* o, void* cuda_stream);
+
+/*
+ * Same step with HOST buffers (same layouts): copies q/k/v into the handle's
+ * device staging, runs the step and copies o back, all enqueued on
+ * cuda_stream.  Host buffers should be page-locked for the copies to be
+ * asynchronous; they must stay valid and unmodified until the stream passes
+ * the call.
+ */
+int statekv_prefill_frame_host(statekv_handle* h, const void* q_host,
+                               const void* k_host, const void* v_host,
+                               void* o_host, void* cuda_stream);
+
+/*
+ * Borrowed DEVICE pointers to the compressed state C_{n-1} of (stream s,
+ * layer) after the last step: k, v -> [Hkv][pitch][d], pos -> [Hkv][pitch]
+ * int32 virtual positions; the first *count slots of each head are live
+ * (count = min(B, n*T)), in slot order.  *pitch = B + T.  Valid until the
+ * next call that changes the handle.  Any output pointer may be NULL.
+ */
+int statekv_get_compressed(statekv_handle* h, int32_t s, int32_t layer,
+                           const void** k, const void** v, const int32_t** pos,
+                           int32_t* count, int32_t* pitch);
+
+/*
+ * Borrowed DEVICE pointers to the detailed state D_{n-1} of (s, layer):
+ * k, v -> [Hkv][pitch][d] with row r = virtual position r - position_offset
+ * (post-RoPE K, V as given); *count = n*T live rows per head,
+ * *pitch = max_frames*T.  Any output pointer may be NULL.
+ */
+int statekv_get_detailed(statekv_handle* h, int32_t s, int32_t layer,
+                         const void** k, const void** v, int64_t* count,
+                         int64_t* pitch);
+
+/* Frames processed so far (n). */
+int64_t statekv_frame_index(const statekv_handle* h);
+
+/* Forget all frames: n = 0, c = 0 (allocations kept, contents stale). */
+int statekv_reset(statekv_handle* h);
+
+/*
+ * Synchronise cuda_stream, then report and clear the device status word:
+ * STATEKV_OK, STATEKV_E_TIMEOUT (a bounded wait inside a kernel gave up; that
+ * launch's outputs are invalid) or STATEKV_E_DEVICE.
+ */
+int statekv_check_device_status(statekv_handle* h, void* cuda_stream);
+
+/* ------------------------------------------------------------- test hooks */
+
+/*
+ * Importance scores of the last step (关键设计 2) for (s, layer):
+ * scores -> [Hkv][pitch] fp32, pool_pos -> [Hkv][pitch] int32, both in pool
+ * slot order before the Top-B update (slots [0,c) held C_{n-1}, slots
+ * [c, c+T) the frame's tokens); *m = c + T candidates.  Borrowed DEVICE
+ * pointers, valid until the next step.
+ */
+int statekv_get_scores(statekv_handle* h, int32_t s, int32_t layer,
+                       const float** scores, const int32_t** pool_pos,
+                       int32_t* m, int32_t* pitch);
+
+/* Borrowed DEVICE pointer to the last step's rotated queries Q'
+ * ([S][L][Hq][T][d], storage dtype). */
+int statekv_get_rotated_query(statekv_handle* h, const void** q_rot);
+
+/* Set the frame index n (teacher forcing / resume); 0 <= n < max_frames. */
+int statekv_set_frame_index(statekv_handle* h, int64_t n);
+
+/*
+ * Teacher forcing / resume: overwrite C of (s, layer) with count rows per KV
+ * head from DEVICE buffers k, v [Hkv][count][d] (post-RoPE, storage dtype)
+ * and pos [Hkv][count] int32.  count must equal min(B, n*T) for the current
+ * frame index n.  Copies are enqueued on cuda_stream.
+ */
+int statekv_set_compressed(statekv_handle* h, int32_t s, int32_t layer,
+                           const void* k, const void* v, const int32_t* pos,
+                           int32_t count, void* cuda_stream);
+
+/*
+ * Per-kernel timing with CUDA events recorded on the launch stream around
+ * every launch while enabled.  statekv_profile_read synchronises, then
+ * returns for kernel id (STATEKV_KERNEL_*) the summed device milliseconds
+ * and the number of launches since profiling was last enabled.
+ */
+int statekv_profile_enable(statekv_handle* h, int enable);
+int statekv_profile_read(statekv_handle* h, int32_t kernel, double* total_ms,
+                         int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STATEKV_H_ */

@@ -1,0 +1,141 @@
+// RoPE at virtual stream positions, with the detailed-state append fused in.
+//
+// StateKV ("Linear Scaling Video VLMs for Long Video Understanding"),
+// 关键设计 3: every rotation angle uses the logical position L_n = nT (+ i) of
+// the token in the stream, with one global scale alpha fixed for the whole
+// run; 关键设计 1: the frame's K/V go to the detailed state D_n and join the
+// candidate pool next to the compressed state.
+//
+// Two kernels per frame:
+//  * rope_table: cos/sin of p*omega_k for the frame's T positions.  The angle
+//    reaches ~1.3e5 rad at 512 frames, where an fp32 product p*omega loses
+//    ~1e-2 rad, so the product and the reduction to [-pi, pi] are done in
+//    fp64 (T*d/2 angles per frame, shared by every head and layer);
+//  * rope: one pass over Q, K and V of all (stream, layer, head) rows.
+//    Q' goes to scratch; K' and V go to the compressed pool after its c live
+//    slots and to D rows [nT, nT+T).  16-byte vector loads/stores, rows of
+//    d/2 + d/2 pairs handled by d/(2*VEC) threads each.
+#include "statekv_internal.cuh"
+
+namespace statekv {
+namespace {
+
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+
+__global__ void rope_table_kernel(RopeTableArgs a) {
+    int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    int total = a.T * a.half;
+    if (idx >= total) return;
+    int i = idx / a.half;
+    int k = idx - i * a.half;
+    double ang = (double)(a.p0 + i) * a.omega[k];
+    double turns = rint(ang * (1.0 / kTwoPi));
+    double r = fma(-turns, kTwoPi, ang);          // in [-pi, pi] (+ rounding)
+    float s, c;
+    sincosf((float)r, &s, &c);
+    a.cs[idx] = make_float2(c, s);
+}
+
+template <typename E> struct Vec;
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void load(const void* p, float (&x)[N]) {
+        uint4 u = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j) {
+            float2 f = __bfloat1622float2(h[j]);
+            x[2 * j] = f.x; x[2 * j + 1] = f.y;
+        }
+    }
+    __device__ static uint4 pack(const float (&x)[N]) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j) h[j] = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+        return u;
+    }
+};
+template <> struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ static void load(const void* p, float (&x)[N]) {
+        float4 f = *reinterpret_cast<const float4*>(p);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    }
+    __device__ static uint4 pack(const float (&x)[N]) {
+        float4 f = make_float4(x[0], x[1], x[2], x[3]);
+        return *reinterpret_cast<uint4*>(&f);
+    }
+};
+
+template <typename E>
+__global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
+    constexpr int VEC = Vec<E>::N;
+    const int half = a.d / 2;
+    const int tpr = half / VEC;                      // threads per row
+    int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t row = gid / tpr;
+    int j = (int)(gid - row * tpr);
+    int64_t total = a.rows_q + 2 * a.rows_kv;
+    if (row >= total) return;
+    const int k0 = j * VEC;
+
+    const E* src;
+    int64_t src_row;
+    int kind;                                        // 0 = Q, 1 = K, 2 = V
+    if (row < a.rows_q) { kind = 0; src = (const E*)a.q; src_row = row; }
+    else if (row < a.rows_q + a.rows_kv) { kind = 1; src = (const E*)a.k; src_row = row - a.rows_q; }
+    else { kind = 2; src = (const E*)a.v; src_row = row - a.rows_q - a.rows_kv; }
+    const int i = (int)(src_row % a.T);              // token index in the frame
+
+    float x[VEC], y[VEC];
+    const E* base = src + src_row * a.d;
+    Vec<E>::load(base + k0, x);
+    Vec<E>::load(base + half + k0, y);
+    if (kind != 2) {
+        const float2* cs = a.cs + (int64_t)i * half + k0;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            float2 t = cs[e];
+            float xr = fmaf(x[e], t.x, -y[e] * t.y);
+            float yr = fmaf(y[e], t.x, x[e] * t.y);
+            x[e] = xr; y[e] = yr;
+        }
+    }
+    uint4 lo = Vec<E>::pack(x), hi = Vec<E>::pack(y);
+    if (kind == 0) {
+        E* dst = (E*)a.q_rot + src_row * a.d;
+        *reinterpret_cast<uint4*>(dst + k0) = lo;
+        *reinterpret_cast<uint4*>(dst + half + k0) = hi;
+        return;
+    }
+    const int64_t unit = src_row / a.T;
+    E* pool = (E*)(kind == 1 ? a.pool_k : a.pool_v) + (unit * a.slots + a.c + i) * a.d;
+    E* det = (E*)(kind == 1 ? a.det_k : a.det_v) + (unit * a.det_pitch + a.det_row0 + i) * a.d;
+    *reinterpret_cast<uint4*>(pool + k0) = lo;
+    *reinterpret_cast<uint4*>(pool + half + k0) = hi;
+    *reinterpret_cast<uint4*>(det + k0) = lo;
+    *reinterpret_cast<uint4*>(det + half + k0) = hi;
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st) {
+    int total = a.T * a.half;
+    rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st) {
+    int vec = dtype == STATEKV_BF16 ? 8 : 4;
+    int64_t threads = (a.rows_q + 2 * a.rows_kv) * (a.d / 2 / vec);
+    int64_t blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (dtype == STATEKV_BF16)
+        rope_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(a);
+    else
+        rope_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace statekv

@@ -1,0 +1,203 @@
+// Score finish, Top-B selection and the in-place compressed-state update.
+//
+// StateKV ("Linear Scaling Video VLMs for Long Video Understanding"),
+// 关键设计 2: the candidate pool U_n is the compressed state's tokens plus the
+// frame's T tokens; each candidate j is scored by the mean attention the
+// frame's queries paid to it, s_j; S̄_n = TopK({s_j}, B) forms C_n.
+//
+// One CTA per (stream, layer, KV head):
+//   1. s_j = (sum over query-row tiles of the column sums of P) / (G*T), in a
+//      fixed tile order (deterministic);
+//   2. every candidate gets the 64-bit key (float bits of s_j) << 32 |
+//      ~position: s_j >= 0, so the bit pattern orders like the value, and the
+//      complemented position makes the lower position win a tie.  Keys are
+//      distinct, so "keep the B largest keys" is exactly Top-B with the tie
+//      rule;
+//   3. an MSB-first radix select (8 passes of 8 bits, shared histogram with
+//      warp-aggregated increments) finds the E-th smallest key, E = m - B;
+//      keys at or below it are evicted;
+//   4. slot reuse: the pool is [compressed slots 0..c) ; frame rows c..c+T).
+//      Evicted slots below B ("holes") are refilled by surviving rows at or
+//      above B ("movers"), paired in slot order; only those rows move
+//      (<= T rows of K and V per unit instead of rewriting all B).
+#include "statekv_internal.cuh"
+
+namespace statekv {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__device__ __forceinline__ uint64_t cand_key(float s, int32_t pos) {
+    return ((uint64_t)__float_as_uint(s) << 32) | (uint64_t)(0xffffffffu - (uint32_t)pos);
+}
+
+__global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);          // [m]
+    int32_t* holes = reinterpret_cast<int32_t*>(keys + a.slots);     // [T]
+    int32_t* movers = holes + a.T;                                   // [T]
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t warp_tot[2][kThreads / 32];
+    __shared__ uint64_t s_prefix;
+    __shared__ uint32_t s_rank;
+
+    const int u = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int c = a.c, T = a.T, B = a.B;
+    const int m = c + T;
+    int32_t* pos = a.pos + (int64_t)u * a.slots;
+
+    // ---- 1-2. scores, positions, keys
+    const float* cs = a.colsum + (int64_t)u * a.n_row_tiles * a.m_pad;
+    float* scores = a.scores + (int64_t)u * a.m_pad;
+    int32_t* spos = a.score_pos + (int64_t)u * a.m_pad;
+    for (int j = tid; j < m; j += kThreads) {
+        float acc = 0.f;
+        for (int t = 0; t < a.n_row_tiles; ++t) acc += cs[(int64_t)t * a.m_pad + j];
+        float s = acc * a.inv_rows;
+        int32_t p = j < c ? pos[j] : a.pos_base + (j - c);
+        scores[j] = s;
+        spos[j] = p;
+        keys[j] = cand_key(s, p);
+    }
+    if (m <= B) {                               // state not full: keep all
+        for (int j = c + tid; j < m; j += kThreads) pos[j] = a.pos_base + (j - c);
+        return;
+    }
+    __syncthreads();
+
+    // ---- 3. radix select of the E-th smallest key
+    const uint32_t E = (uint32_t)(m - B);
+    if (tid == 0) { s_prefix = 0ull; s_rank = E; }
+    for (int pass = 0; pass < 8; ++pass) {
+        const int shift = 56 - 8 * pass;
+        if (tid < 256) hist[tid] = 0u;
+        __syncthreads();
+        const uint64_t prefix = s_prefix;
+        for (int j0 = 0; j0 < m; j0 += kThreads) {
+            int j = j0 + tid;
+            bool act = false;
+            uint32_t dig = 0;
+            if (j < m) {
+                uint64_t k = keys[j];
+                act = (pass == 0) || ((k >> (shift + 8)) == (prefix >> (shift + 8)));
+                dig = (uint32_t)(k >> shift) & 255u;
+            }
+            uint32_t amask = __ballot_sync(0xffffffffu, act);
+            if (act) {
+                uint32_t peers = __match_any_sync(amask, dig);
+                if (lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t rank = s_rank;
+            uint32_t h[8], run = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { h[e] = hist[lane * 8 + e]; run += h[e]; }
+            uint32_t incl = run;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            uint32_t excl = incl - run;
+            bool mine = excl < rank && rank <= incl;
+            if (mine) {
+                uint32_t below = excl;
+                int b = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (below + h[e] >= rank) { b = e; break; }
+                    below += h[e];
+                }
+                s_prefix = prefix | ((uint64_t)(lane * 8 + b) << shift);
+                s_rank = rank - below;
+            }
+        }
+        __syncthreads();
+    }
+    const uint64_t kappa = s_prefix;            // E-th smallest key: evict <= kappa
+
+    // ---- 4. holes (slots < B evicted) and movers (slots >= B kept), slot order
+    const int per = (m + kThreads - 1) / kThreads;
+    const int j0 = tid * per, j1 = min(j0 + per, m);
+    uint32_t nh = 0, nm = 0;
+    for (int j = j0; j < j1; ++j) {
+        bool kept = keys[j] > kappa;
+        nh += (j < B && !kept);
+        nm += (j >= B && kept);
+    }
+    // block-wide exclusive scan of (nh, nm)
+    uint32_t ih = nh, im = nm;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        uint32_t yh = __shfl_up_sync(0xffffffffu, ih, off);
+        uint32_t ym = __shfl_up_sync(0xffffffffu, im, off);
+        if (lane >= off) { ih += yh; im += ym; }
+    }
+    if (lane == 31) { warp_tot[0][warp] = ih; warp_tot[1][warp] = im; }
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t th = warp_tot[0][lane], tm = warp_tot[1][lane];
+        uint32_t ph = th, pm = tm;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            uint32_t yh = __shfl_up_sync(0xffffffffu, ph, off);
+            uint32_t ym = __shfl_up_sync(0xffffffffu, pm, off);
+            if (lane >= off) { ph += yh; pm += ym; }
+        }
+        warp_tot[0][lane] = ph - th;
+        warp_tot[1][lane] = pm - tm;
+    }
+    __syncthreads();
+    uint32_t oh = warp_tot[0][warp] + ih - nh;
+    uint32_t om = warp_tot[1][warp] + im - nm;
+    for (int j = j0; j < j1; ++j) {
+        bool kept = keys[j] > kappa;
+        if (j < B && !kept) holes[oh++] = j;
+        if (j >= B && kept) movers[om++] = j;
+        // surviving frame rows that stay in place get their position
+        if (kept && j >= c && j < B) pos[j] = a.pos_base + (j - c);
+    }
+    // the last thread's end offsets are the totals; every hole gets a mover
+    __shared__ uint32_t s_pairs;
+    if (tid == kThreads - 1) {
+        s_pairs = min(oh, om);
+        if (oh != om) record_error(a.err, (uint32_t)STATEKV_E_DEVICE, kSiteSelect, oh * 65536u + om);
+    }
+    __syncthreads();
+    const uint32_t np = s_pairs;
+    for (uint32_t r = tid; r < np; r += kThreads) pos[holes[r]] = a.pos_base + (movers[r] - c);
+
+    // ---- row moves (K and V), 16-byte vectors
+    const int vpr = a.row_bytes / 16;
+    const int64_t unit_bytes = (int64_t)a.slots * a.row_bytes;
+    uint4* pk = reinterpret_cast<uint4*>((char*)a.pool_k + u * unit_bytes);
+    uint4* pv = reinterpret_cast<uint4*>((char*)a.pool_v + u * unit_bytes);
+    const int64_t total = (int64_t)np * vpr;
+    for (int64_t e = tid; e < total; e += kThreads) {
+        int r = (int)(e / vpr), w = (int)(e - (int64_t)r * vpr);
+        int64_t dst = (int64_t)holes[r] * vpr + w, src = (int64_t)movers[r] * vpr + w;
+        pk[dst] = pk[src];
+        pv[dst] = pv[src];
+    }
+}
+
+}  // namespace
+
+size_t select_smem_bytes(int slots, int T) {
+    return (size_t)slots * sizeof(uint64_t) + 2 * (size_t)T * sizeof(int32_t);
+}
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
+    size_t smem = select_smem_bytes(a.slots, a.T);
+    cudaError_t e = cudaFuncSetAttribute(select_kernel,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_kernel<<<a.U, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace statekv

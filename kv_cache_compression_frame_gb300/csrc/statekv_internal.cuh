@@ -1,0 +1,108 @@
+// Internal declarations shared by the libstatekv translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "statekv.h"
+
+namespace statekv {
+
+// Device status word layout (uint32[4]): [0] status code (STATEKV_E_*),
+// [1] site id of the first failure, [2] blockIdx.x, [3] extra.
+constexpr int kErrWords = 4;
+
+// Error sites recorded by bounded waits.
+enum ErrSite : uint32_t {
+    kSiteQFull = 1, kSiteKvFull, kSiteKvEmpty, kSiteSFull, kSiteSEmpty,
+    kSitePFull, kSitePEmpty, kSiteOFull, kSiteDrain, kSiteTmemAddr, kSiteCol,
+    kSiteSelect = 32,
+};
+
+// ------------------------------------------------------------- launchers
+struct RopeArgs {
+    const void* q; const void* k; const void* v;   // caller inputs
+    void* q_rot;                                   // [U*G*T][d]
+    void* pool_k; void* pool_v;                    // [U][slots][d]
+    void* det_k; void* det_v;                      // [U][det_pitch][d]
+    const float2* cs;                              // [T][d/2] (cos, sin)
+    int64_t rows_q;      // S*L*Hq*T
+    int64_t rows_kv;     // S*L*Hkv*T
+    int32_t T, d, slots, c;
+    int64_t det_pitch, det_row0;                   // det row of token 0 = n*T
+};
+
+struct RopeTableArgs {
+    const double* omega;  // [d/2]
+    float2* cs;           // [T][d/2]
+    int64_t p0;           // virtual position of token 0 of this frame
+    int32_t T, half;
+};
+
+struct AttnArgs {
+    const void* q_rot;    // [U][GT][d]
+    const void* pool_k;   // [U][slots][d]
+    const void* pool_v;
+    void* o;              // [U][GT][d]
+    float* colsum;        // [U][n_row_tiles][m_pad] per-tile key column sums of P
+    uint32_t* err;
+    int32_t U, GT, T, d, slots, c, m_pad, n_row_tiles;
+    float scale_log2;     // mscale^2/sqrt(d) * log2(e)
+    float scale;          // mscale^2/sqrt(d)
+};
+
+struct SelectArgs {
+    const float* colsum;  // [U][n_row_tiles][m_pad]
+    float* scores;        // [U][m_pad]
+    int32_t* score_pos;   // [U][m_pad]
+    int32_t* pos;         // [U][slots] live positions of the compressed pool
+    void* pool_k; void* pool_v;   // [U][slots][row_bytes]
+    uint32_t* err;
+    int32_t U, n_row_tiles, m_pad, slots, c, T, B, row_bytes;
+    int32_t pos_base;     // virtual position of this frame's token 0
+    float inv_rows;       // 1 / (G*T)
+};
+
+cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st);
+cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tm_q,
+                                const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                cudaStream_t st);
+cudaError_t launch_attention_simt(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
+
+// Query-row tile heights of the two attention paths (the column-sum buffer
+// holds one row of partial sums per tile).
+constexpr int kTcRowTile = 128;
+constexpr int kSimtRowTile = 16;
+// Dynamic shared memory of the select kernel for B + T candidates.
+size_t select_smem_bytes(int slots, int T);
+constexpr int kMaxSlots = 24576;
+
+}  // namespace statekv
+
+// ---------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+namespace statekv {
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Record the first device-side failure; later ones are dropped.
+__device__ __forceinline__ void record_error(uint32_t* err, uint32_t code,
+                                             uint32_t site, uint32_t extra) {
+    if (atomicCAS(err, 0u, code) == 0u) {
+        err[1] = site;
+        err[2] = blockIdx.x;
+        err[3] = extra;
+        __threadfence();
+    }
+}
+
+}  // namespace statekv
+#endif

@@ -1,0 +1,272 @@
+"""GPU parity of the CUDA path against the CPU oracle, one frame step at a
+time, through the C ABI (Python binding).
+
+Every checked step compares: RoPE of Q and K (ulp), the D append (bit-exact
+K' copy and V copy), O (row-relative error), the scores s_j, the Top-B
+selection (up to near-ties) and the slot-reuse gather into C (bit-exact).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.statekv_oracle as orc
+from synth import SHAPES, FrameSource, WorkloadShape
+from parity import (O_TOL, check_rope, check_scores, check_selection, f64,
+                    raw_equal, row_rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kv_cache_compression_frame_gb300 import build_lib
+    build_lib.build()
+
+
+def _small(name, **kw) -> WorkloadShape:
+    base = dict(name=name, streams=1, layers=1, q_heads=2, kv_heads=1,
+                head_dim=64, frame_tokens=16, budget=32, frames=8,
+                rope_theta=1e4, rope_alpha=1.0, rope_orig_ctx=0, dtype="bf16",
+                sinks_per_frame=2, sink_gain=3.0, sink_drift=0.05,
+                key_scale_sigma=0.0)
+    base.update(kw)
+    return WorkloadShape(**base)
+
+
+class Stepper:
+    """Runs the CUDA path frame by frame and checks steps against the oracle."""
+
+    def __init__(self, shape: WorkloadShape, position_offset: int = 0):
+        from kv_cache_compression_frame_gb300 import StateKV, StateKVConfig
+        self.sh = shape
+        self.src = FrameSource(shape)
+        self.offset = position_offset
+        self.h = StateKV(StateKVConfig.from_shape(shape, position_offset=position_offset))
+        self.dev = self.h.device
+        self.tdt = self.h.torch_dtype
+        self.omega, ms = orc.rope_frequencies(shape.head_dim, shape.rope_theta,
+                                              shape.rope_alpha, shape.rope_orig_ctx)
+        self.scale = orc.logit_scale(shape.head_dim, ms)
+        self.stats = []
+
+    def tensors(self, n):
+        q, k, v = self.src.frame(n)
+        t = [torch.from_numpy(a).to(self.tdt).to(self.dev) for a in (q, k, v)]
+        return (q, k, v), t
+
+    def run(self, n):
+        _, (q, k, v) = self.tensors(n)
+        o = self.h.prefill_frame(q, k, v)
+        self.h.check_device_status()
+        return o
+
+    def step(self, n, units=None):
+        sh, h = self.sh, self.h
+        assert h.frame_index == n
+        T, G, B = sh.frame_tokens, sh.group, sh.budget
+        (qn, kn, vn), (q, k, v) = self.tensors(n)
+        if units is None:
+            units = [(s, l, hk) for s in range(sh.streams) for l in range(sh.layers)
+                     for hk in range(sh.kv_heads)]
+        pre = {}
+        for (s, l) in {(s, l) for s, l, _ in units}:
+            ck, cv, cp, cnt = h.compressed(s, l)
+            pre[(s, l)] = (ck[:, :cnt].clone().cpu(), cv[:, :cnt].clone().cpu(),
+                           cp[:, :cnt].clone().cpu().numpy(), cnt)
+        o = h.prefill_frame(q, k, v)
+        h.check_device_status()
+        pos = self.offset + n * T + np.arange(T, dtype=np.int64)
+        # RoPE of every query row
+        q_ref = orc.round_to_storage(orc.rope_rotate(qn, pos, self.omega), sh.dtype)
+        qrot = h.rotated_query().clone().cpu()
+        rq = check_rope(qrot, q_ref, sh.dtype, f"Q' frame {n}")
+        o_cpu = o.cpu()
+        worst = dict(o=0.0, s=0.0, swaps=0, rope_q=rq)
+        for (s, l, hk) in units:
+            what = f"frame {n} unit ({s},{l},{hk})"
+            dk, dv, dcnt = h.detailed(s, l)
+            assert dcnt == (n + 1) * T
+            krot = dk[hk, n * T:(n + 1) * T].clone().cpu()
+            check_rope(krot, orc.round_to_storage(orc.rope_rotate(kn[s, l, hk], pos, self.omega),
+                                                  sh.dtype), sh.dtype, f"K' {what}")
+            assert raw_equal(dv[hk, n * T:(n + 1) * T].cpu(), v[s, l, hk].cpu()), f"D V {what}"
+            ck, cv, cp, cnt = pre[(s, l)]
+            pool_k_raw = torch.cat([ck[hk], krot])
+            pool_v_raw = torch.cat([cv[hk], v[s, l, hk].cpu()])
+            pool_pos = np.concatenate([cp[hk].astype(np.int64), pos])
+            qr = f64(qrot[s, l, hk * G:(hk + 1) * G])
+            O_ref, P = orc.attend_frame(qr, f64(pool_k_raw), f64(pool_v_raw), cnt, self.scale)
+            s_ref = orc.importance_scores(P)
+            e = row_rel_err(f64(o_cpu[s, l, hk * G:(hk + 1) * G]), O_ref)
+            assert e <= O_TOL[sh.dtype], f"O {what}: row-relative error {e:.3g}"
+            worst["o"] = max(worst["o"], e)
+            sc, sp, m = h.scores(s, l)
+            assert m == cnt + T
+            np.testing.assert_array_equal(sp[hk, :m].cpu().numpy(), pool_pos)
+            worst["s"] = max(worst["s"], check_scores(f64(sc[hk, :m]), s_ref, f"s {what}"))
+            nk, nv, npos, ncnt = h.compressed(s, l)
+            assert ncnt == min(B, cnt + T)
+            kept = npos[hk, :ncnt].cpu().numpy().astype(np.int64)
+            worst["swaps"] += check_selection(kept, s_ref, pool_pos, B, f"select {what}")
+            # slot-reuse gather: every live slot is a bit copy of its pool row
+            where = {int(p): i for i, p in enumerate(pool_pos)}
+            idx = torch.tensor([where[int(p)] for p in kept], dtype=torch.long)
+            assert raw_equal(nk[hk, :ncnt].cpu(), pool_k_raw[idx]), f"C K gather {what}"
+            assert raw_equal(nv[hk, :ncnt].cpu(), pool_v_raw[idx]), f"C V gather {what}"
+        self.stats.append((n, worst))
+        return worst
+
+
+# ------------------------------------------------------------------- tests
+def test_tiny_f32_every_frame():
+    st = Stepper(SHAPES["tiny_f32"])
+    for n in range(SHAPES["tiny_f32"].frames):
+        st.step(n)
+
+
+def test_ragged_bf16_partial_fill():
+    # G*T = 144 rows: two query tiles, the second ragged and spanning heads;
+    # B = 100 is not a multiple of T, so frame 2 evicts while C is filling
+    sh = _small("ragged", layers=2, q_heads=6, kv_heads=2, head_dim=64,
+                frame_tokens=48, budget=100, frames=6)
+    st = Stepper(sh)
+    for n in range(sh.frames):
+        st.step(n)
+
+
+def test_d128_streams_layers_offset_yarn():
+    sh = _small("multi", streams=2, layers=2, q_heads=4, kv_heads=2, head_dim=128,
+                frame_tokens=64, budget=192, frames=6, rope_theta=1e6,
+                rope_alpha=4.0, rope_orig_ctx=200, key_scale_sigma=0.5)
+    st = Stepper(sh, position_offset=1000)
+    for n in range(sh.frames):
+        st.step(n)
+
+
+def test_zero_budget_is_per_frame_attention():
+    sh = _small("b0", q_heads=4, kv_heads=2, head_dim=64, frame_tokens=80, budget=0, frames=3)
+    st = Stepper(sh)
+    for n in range(3):
+        st.step(n)
+        _, _, _, cnt = st.h.compressed(0, 0)
+        assert cnt == 0
+
+
+def test_internvl3_1b_layer_through_fill_to_steady_state():
+    sh = SHAPES["internvl3_1b_layer"]
+    st = Stepper(sh)
+    for n in range(18):
+        if n in (0, 1, 15, 16, 17):
+            st.step(n)
+        else:
+            st.run(n)
+
+
+@pytest.mark.parametrize("name,layers", [("internvl3_2b_stack", (0, 13, 27)),
+                                         ("qwen3vl_2b_stack", (0, 27))])
+def test_full_size_steady_state_sampled(name, layers):
+    """The workload bench.py times, at full size: all layers run; the step at
+    frame 16 (state full, c = B) is checked on sampled layers."""
+    sh = SHAPES[name]
+    st = Stepper(sh)
+    for n in range(16):
+        st.run(n)
+    units = [(0, l, hk) for l in layers for hk in range(sh.kv_heads)]
+    st.step(16, units=units)
+
+
+def test_teacher_forced_from_oracle_state():
+    """C_{n-1} taken from the oracle's own free-running state."""
+    sh = SHAPES["internvl3_1b_layer"].with_(frames=20)
+    src = FrameSource(sh)
+    ref = orc.StateKVOracle(sh)
+    for n in range(17):
+        ref.prefill_frame(*src.frame(n))
+    st = Stepper(sh)
+    st.h.set_frame_index(17)
+    u = [ref.units[(0, 0, hk)] for hk in range(sh.kv_heads)]
+    dt = st.tdt
+    k = torch.from_numpy(np.stack([x.comp_k for x in u])).to(dt).cuda()
+    v = torch.from_numpy(np.stack([x.comp_v for x in u])).to(dt).cuda()
+    p = torch.from_numpy(np.stack([x.comp_pos for x in u]).astype(np.int32)).cuda()
+    st.h.set_compressed(0, 0, k, v, p)
+    torch.cuda.synchronize()
+    st.step(17)
+
+
+def test_free_running_selection_overlap():
+    """End to end: the GPU and the oracle each run on their own state; the
+    per-frame overlap of the kept position sets is reported."""
+    sh = SHAPES["internvl3_1b_layer"].with_(frames=40)
+    src = FrameSource(sh)
+    ref = orc.StateKVOracle(sh)
+    st = Stepper(sh)
+    overlaps = []
+    for n in range(sh.frames):
+        q, k, v = src.frame(n)
+        ref.prefill_frame(q, k, v)
+        st.run(n)
+        if (n + 1) * sh.frame_tokens > sh.budget:
+            for hk in range(sh.kv_heads):
+                _, _, p, c = st.h.compressed(0, 0)
+                got = set(p[hk, :c].cpu().numpy().tolist())
+                want = set(ref.units[(0, 0, hk)].comp_pos.tolist())
+                overlaps.append(len(got & want) / sh.budget)
+    print("selection overlap: min %.4f mean %.4f" % (min(overlaps), float(np.mean(overlaps))))
+    assert float(np.mean(overlaps)) > 0.9
+
+
+def test_capacity_is_rejected_and_state_kept():
+    from kv_cache_compression_frame_gb300 import StateKVError
+    sh = _small("cap", frames=2)
+    st = Stepper(sh)
+    st.run(0)
+    st.run(1)
+    _, (q, k, v) = st.tensors(2)
+    with pytest.raises(StateKVError) as ei:
+        st.h.prefill_frame(q, k, v)
+    assert ei.value.status == -3
+    assert st.h.frame_index == 2
+
+
+def test_host_entry_point_matches_device_entry_point():
+    sh = _small("host", q_heads=4, kv_heads=2, head_dim=128, frame_tokens=64,
+                budget=128, frames=4)
+    a, b = Stepper(sh), Stepper(sh)
+    for n in range(4):
+        _, (q, k, v) = a.tensors(n)
+        oa = a.h.prefill_frame(q, k, v)
+        ob = torch.empty(oa.shape, dtype=oa.dtype).pin_memory()
+        b.h.prefill_frame_host(q.cpu().pin_memory(), k.cpu().pin_memory(),
+                               v.cpu().pin_memory(), ob)
+        torch.cuda.synchronize()
+        assert raw_equal(oa.cpu(), ob)
+        ka, _, pa, ca = a.h.compressed(0, 0)
+        kb, _, pb, cb = b.h.compressed(0, 0)
+        assert ca == cb and torch.equal(pa[:, :ca], pb[:, :cb])
+        assert raw_equal(ka[:, :ca], kb[:, :cb])
+
+
+def test_reset_replays_bit_identically():
+    sh = _small("replay", q_heads=4, kv_heads=2, head_dim=64, frame_tokens=64,
+                budget=96, frames=4)
+    st = Stepper(sh)
+    first = [st.run(n).cpu() for n in range(4)]
+    st.h.reset()
+    again = [st.run(n).cpu() for n in range(4)]
+    for x, y in zip(first, again):
+        assert raw_equal(x, y)
+
+
+def test_profile_counts_every_launch():
+    sh = _small("prof", frames=3)
+    st = Stepper(sh)
+    st.h.profile_enable(True)
+    for n in range(3):
+        st.run(n)
+    prof = st.h.profile_read()
+    assert all(cnt == 3 for _, cnt in prof.values()), prof
+    assert all(ms > 0 for ms, _ in prof.values()), prof
