@@ -82,7 +82,7 @@ class Stepper:
         # RoPE of every query row
         q_ref = orc.round_to_storage(orc.rope_rotate(qn, pos, self.omega), sh.dtype)
         qrot = h.rotated_query().clone().cpu()
-        rq = check_rope(qrot, q_ref, sh.dtype, f"Q' frame {n}")
+        rq = check_rope(qrot, q_ref, qn, sh.dtype, f"Q' frame {n}")
         o_cpu = o.cpu()
         worst = dict(o=0.0, s=0.0, swaps=0, rope_q=rq)
         for (s, l, hk) in units:
@@ -91,7 +91,7 @@ class Stepper:
             assert dcnt == (n + 1) * T
             krot = dk[hk, n * T:(n + 1) * T].clone().cpu()
             check_rope(krot, orc.round_to_storage(orc.rope_rotate(kn[s, l, hk], pos, self.omega),
-                                                  sh.dtype), sh.dtype, f"K' {what}")
+                                                  sh.dtype), kn[s, l, hk], sh.dtype, f"K' {what}")
             assert raw_equal(dv[hk, n * T:(n + 1) * T].cpu(), v[s, l, hk].cpu()), f"D V {what}"
             ck, cv, cp, cnt = pre[(s, l)]
             pool_k_raw = torch.cat([ck[hk], krot])
