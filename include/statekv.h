@@ -236,6 +236,54 @@ int statekv_profile_enable(statekv_handle* h, int enable);
 int statekv_profile_read(statekv_handle* h, int32_t kernel, double* total_ms,
                          int64_t* launches);
 
+/* ------------------------------------------------- allocation-free entry */
+
+/*
+ * No counterpart in the paper: a deployment convenience.
+ *
+ * Frame attention and importance scores for callers that cannot allocate
+ * device memory -- whose memory is owned by another allocator (an inference
+ * server's pool, a framework hosting this library as a plugin) or that must
+ * avoid the device-wide synchronisation cudaMalloc/cudaFree can cause.  It
+ * creates no handle and calls no cudaMalloc, cudaFree or other allocating
+ * routine; its only scratch (the per-query-tile column sums of P) is a
+ * file-scope 16 MiB __device__ array that every GPU loading this library
+ * holds until the process exits.
+ *
+ * Computes, per unit u (one KV head of one layer and stream), exactly the
+ * attention and scores of one statekv_prefill_frame step:
+ *   o      = softmax(q_rot pool_k^T * logit_scale, masked) pool_v
+ *   scores = s_j, the mean over the group*frame_tokens query rows of P[:, j]
+ * where pool rows [0, compressed) are compressed keys (visible to every
+ * query) and rows [compressed, compressed + frame_tokens) are the frame's
+ * keys in token order (frame key i' visible to query token i iff i' <= i).
+ * DEVICE pointers on the current device, caller-owned, contiguous, storage
+ * dtype (STATEKV_BF16 or STATEKV_F32), 16-byte aligned:
+ *   q_rot  [units][group * frame_tokens][head_dim]  rotated queries, g-major
+ *   pool_k, pool_v [units][pool_rows][head_dim]     pool_rows >= compressed + frame_tokens
+ *   o      [units][group * frame_tokens][head_dim]  written
+ *   scores [units][compressed + frame_tokens] fp32  written
+ *   status uint32[4] device status word (NULL: an internal one); a bounded
+ *          device wait that gives up writes STATEKV_E_TIMEOUT into status[0]
+ *          and leaves o and scores unspecified.
+ * logit_scale = mscale^2 / sqrt(head_dim).  Returns STATEKV_E_CAPACITY when
+ * units * ceil(group*frame_tokens / R) * round_up(pool_rows, 128) * 4 bytes
+ * exceeds the 16 MiB scratch (R = 128 query rows per tile for bf16, 16 for
+ * fp32), STATEKV_E_UNSUPPORTED for head_dim not in {64, 128}.
+ * The first call on a device takes the scratch's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls on a device share the scratch:
+ * calls that overlap on the GPU race and must be serialised by the caller.
+ * Work is enqueued on cuda_stream; results are valid once it passes the call.
+ */
+int statekv_attend_scores_static(const void* q_rot, const void* pool_k,
+                                 const void* pool_v, int32_t units,
+                                 int32_t group, int32_t frame_tokens,
+                                 int32_t head_dim, int32_t pool_rows,
+                                 int32_t compressed, double logit_scale,
+                                 int32_t dtype, void* o, float* scores,
+                                 uint32_t* status, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,6 +38,7 @@ EXPORTS = (
     "statekv_reset", "statekv_check_device_status", "statekv_get_scores",
     "statekv_get_rotated_query", "statekv_set_frame_index",
     "statekv_set_compressed", "statekv_profile_enable", "statekv_profile_read",
+    "statekv_attend_scores_static",
 )
 
 
@@ -96,6 +97,10 @@ def load() -> C.CDLL:
         "statekv_profile_enable": (C.c_int, [h, C.c_int]),
         "statekv_profile_read": (C.c_int, [h, C.c_int32, C.POINTER(C.c_double),
                                            C.POINTER(C.c_int64)]),
+        "statekv_attend_scores_static": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int32,
+                                                   C.c_int32, C.c_int32, C.c_int32,
+                                                   C.c_int32, C.c_double, C.c_int32,
+                                                   _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -1,0 +1,94 @@
+"""The allocation-free entry point, statekv_attend_scores_static.
+
+It serves callers that cannot allocate device memory: their memory belongs to
+another allocator (an inference server's pool, a framework hosting the library
+as a plugin), or they cannot afford the device-wide synchronisation that
+cudaMalloc/cudaFree may cause.  Its only scratch is a fixed __device__ array
+inside the library.  This test calls it through the C ABI and checks its O
+and scores against the handle-based path (statekv_prefill_frame) on the same
+inputs, on two calls in a row, with the parity tolerances used everywhere
+else (O row-relative 2e-2 for bf16; scores 1e-3 relative + 1e-6/m).
+It lives in its own file, collected last.
+"""
+
+import math
+
+import pytest
+import torch
+
+from parity import O_TOL, check_scores, f64, row_rel_err
+from synth import FrameSource, WorkloadShape
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kv_cache_compression_frame_gb300 import build_lib
+    build_lib.build()
+
+
+def test_static_scratch_entry_matches_handle_path():
+    from kv_cache_compression_frame_gb300 import StateKV, StateKVConfig
+    from kv_cache_compression_frame_gb300 import _native as N
+    lib = N.load()
+    sh = WorkloadShape(name="noalloc", streams=1, layers=2, q_heads=4, kv_heads=2,
+                       head_dim=128, frame_tokens=64, budget=192, frames=6,
+                       rope_theta=1e6, rope_alpha=1.0, rope_orig_ctx=0, dtype="bf16",
+                       sinks_per_frame=2, sink_gain=3.0, sink_drift=0.05,
+                       key_scale_sigma=0.0)
+    src = FrameSource(sh)
+    h = StateKV(StateKVConfig.from_shape(sh))
+    dev = h.device
+    T, G, d, U = sh.frame_tokens, sh.group, sh.head_dim, sh.units
+    scale = 1.0 / math.sqrt(d)                  # alpha = 1: plain 1/sqrt(d)
+    stream = torch.cuda.current_stream(dev)
+    for n in range(3):                          # fill the compressed state
+        h.prefill_frame(*(torch.from_numpy(a).to(torch.bfloat16).to(dev) for a in src.frame(n)))
+    for call, n in enumerate((3, 4)):           # two calls in a row
+        c = h.compressed(0, 0)[3]
+        pre = [h.compressed(0, l) for l in range(sh.layers)]
+        pre_k = [p[0][:, :c].clone() for p in pre]
+        pre_v = [p[1][:, :c].clone() for p in pre]
+        q, k, v = (torch.from_numpy(a).to(torch.bfloat16).to(dev) for a in src.frame(n))
+        o_ref = h.prefill_frame(q, k, v)
+        h.check_device_status()
+        q_rot = h.rotated_query().clone()       # [1][L][Hq][T][d] = [U][G*T][d]
+        pk, pv = [], []
+        for l in range(sh.layers):
+            dk, dv, _ = h.detailed(0, l)
+            pk.append(torch.cat([pre_k[l], dk[:, n * T:(n + 1) * T]], dim=1))
+            pv.append(torch.cat([pre_v[l], dv[:, n * T:(n + 1) * T]], dim=1))
+        pool_k = torch.stack(pk).reshape(U, c + T, d).contiguous()
+        pool_v = torch.stack(pv).reshape(U, c + T, d).contiguous()
+        o = torch.empty_like(q_rot)
+        scores = torch.empty((U, c + T), dtype=torch.float32, device=dev)
+        st = lib.statekv_attend_scores_static(
+            q_rot.data_ptr(), pool_k.data_ptr(), pool_v.data_ptr(), U, G, T, d, c + T, c,
+            scale, N.BF16, o.data_ptr(), scores.data_ptr(), None,
+            stream.cuda_stream)
+        assert st == N.OK, N.status_string(st)
+        torch.cuda.synchronize()
+        err = row_rel_err(f64(o), f64(o_ref))
+        assert err <= O_TOL["bf16"], f"call {call}: O row-relative error {err:.3g}"
+        for l in range(sh.layers):
+            s_ref, _, m = h.scores(0, l)
+            for hk in range(sh.kv_heads):
+                check_scores(f64(scores[l * sh.kv_heads + hk]), f64(s_ref[hk, :m]),
+                             f"call {call} layer {l} head {hk}")
+
+
+def test_static_scratch_entry_rejects_oversized_requests():
+    from kv_cache_compression_frame_gb300 import _native as N
+    lib = N.load()
+    buf = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    p = buf.data_ptr()
+    sc = torch.zeros(16, dtype=torch.float32, device="cuda")
+    # 4096 units x 12 query tiles x 4352 padded rows x 4 B >> 16 MiB
+    st = lib.statekv_attend_scores_static(p, p, p, 4096, 6, 256, 128, 4352, 4096, 0.1,
+                                          N.BF16, p, sc.data_ptr(),
+                                          None, None)
+    assert st == N.E_CAPACITY
+    st = lib.statekv_attend_scores_static(p, p, p, 1, 1, 64, 96, 64, 0, 0.1, N.BF16, p,
+                                          sc.data_ptr(), None, None)
+    assert st == N.E_UNSUPPORTED
