@@ -94,8 +94,14 @@ typedef struct statekv_handle statekv_handle;   /* opaque */
  *                 handle's lifetime (关键设计 3)
  *   rope_orig_ctx YaRN original context L_orig (> 0 when alpha != 1)
  *   position_offset virtual position of the first video token (>= 0)
- * Limits: G*T <= 65536 query rows per unit; B + T <= 28672; positions must
+ * Limits: G*T <= 65536 query rows per unit; B + T <= 24576; positions must
  * fit in int32.
+ * Environment: STATEKV_ATTN_CLUSTER = 2 or 4, read by statekv_create (and by
+ * statekv_attend_scores_static on every call), makes bf16 attention CTAs of
+ * consecutive query tiles of one KV head share each K/V tile by TMA
+ * multicast within a thread-block cluster of that size (fewer L2 reads,
+ * coupled pipelines; results are bit-identical).  Unset or any other value:
+ * one CTA per query tile, the measured-faster default.
  */
 typedef struct statekv_config {
     int32_t num_streams;

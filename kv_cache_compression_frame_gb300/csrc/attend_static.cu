@@ -22,8 +22,6 @@
 // address is taken with cudaGetSymbolAddress once per device, with that
 // device current, on the first call made on it; make that first call before
 // any stream capture.
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "statekv_internal.cuh"
@@ -60,27 +58,6 @@ int scratch_for_device(int dev, StaticScratch** out) {
     }
     *out = &s;
     return STATEKV_OK;
-}
-
-bool encode_tile_map(CUtensorMap* m, const void* base, int d, int64_t rows, int64_t units) {
-    static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    if (!enc) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return false;
-        enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)units};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
 }
 
 // s_j = (sum over query tiles of the column sums) / (G*T), fixed tile order.
@@ -137,12 +114,10 @@ extern "C" int statekv_attend_scores_static(
     a.scale_log2 = (float)(logit_scale * 1.4426950408889634074);
     cudaError_t e;
     if (dtype == STATEKV_BF16) {
-        CUtensorMap tq, tk, tv;
-        if (!encode_tile_map(&tq, q_rot, head_dim, GT, units) ||
-            !encode_tile_map(&tk, pool_k, head_dim, pool_rows, units) ||
-            !encode_tile_map(&tv, pool_v, head_dim, pool_rows, units))
+        TcMaps maps;
+        if (!make_tc_maps(&maps, pool_k, pool_v, head_dim, pool_rows, units, (int)n_row_tiles))
             return STATEKV_E_CUDA;
-        e = launch_attention_tc(a, tq, tk, tv, st);
+        e = launch_attention_tc(a, maps, st);
     } else {
         e = launch_attention_simt(a, st);
     }

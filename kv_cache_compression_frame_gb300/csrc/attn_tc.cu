@@ -10,22 +10,45 @@
 //   整体框架 -- the per-frame cost O(T^2 + BT): the key loop covers only the
 //     B compressed keys and the causally visible part of the frame.
 //
-// One CTA = one 128-row query tile of one (stream, layer, KV head).  Rows are
+// One CTA = one 128-row query tile of one (stream, layer, KV head); rows are
 // (g, i) pairs of the G query heads that share the KV head, g-major.  Two
 // sweeps over the 128-key tiles of the pool:
-//   sweep 1: S = Q K^T (tcgen05, fp32 in TMEM) -> running row max / sum of
-//            exp2 -> per-row log-sum-exp (kept in a register);
-//   sweep 2: S again, P = exp2(S*scale - lse) (final, normalised), column
-//            sums of fp32 P (warp reduce-scatter by shuffles, then across the
-//            4 epilogue warps in shared memory), P -> bf16 -> shared memory
-//            (K-major, 128B swizzle) -> O += P V on tcgen05 (V read MN-major).
-// P is normalised by the global lse before PV, so O needs no rescaling.
+//   sweep 1: S = Q K^T (tcgen05, fp32 in TMEM) -> per-thread running max and
+//            sum of exp2 over the thread's columns, combined across the
+//            row's threads at the end -> log-sum-exp per row;
+//   sweep 2: S again, P = exp2(S*scale - lse) (final, normalised): column
+//            sums of fp32 P, and P -> bf16 into TMEM as the A operand of
+//            O += P V (tcgen05 with A in TMEM, V read MN-major from shared
+//            memory).  P is normalised before PV, so O needs no rescaling.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer (one thread), warps 2..5 epilogue (TMEM lanes 32*(w%4)..+31).
-// TMEM (512 columns): S double buffer at 0 and 128, O at 256.
+// Warp roles (576 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// single-thread MMA issuer, warps 2..17 softmax.  Softmax warp w covers TMEM
+// lane quarter w % 4 (the only lanes it may access) and 32-column chunk
+// (w - 2) / 4 of every S tile; with the 16x256b load shape a thread holds
+// 4 rows x 8 columns, so row statistics combine across 4 lanes (then across
+// the 4 chunk warps once per sweep) and column sums need a 3-level shuffle
+// reduction (then across the 4 lane quarters in shared memory, one tile
+// behind, so no warp waits for the others within a tile).
+// Shared-memory bandwidth (128 B/clk/SM) is the scarce resource: an MMA with
+// both operands in shared memory at M = N = 128 consumes all of it, leaving
+// nothing for the TMA writes of the next K/V tiles.  So Q lives in TMEM: the
+// softmax warps copy it there once, and both products read one operand from
+// TMEM (S = Q K^T: Q; O += P V: P) and only K or V from shared memory, which
+// halves the MMA's share of the bandwidth.
+// TMEM (512 columns): Q (bf16 pairs) at 448..; sweep 1 -- three S buffers
+// (0, 128, 256); sweep 2 -- one S buffer (0..127), O (128..), P double buffer
+// (256..383, bf16 pairs).  An S buffer is handed back to the MMA issuer as
+// soon as its tile has been loaded into registers, so S(t+1) is computed
+// while the softmax works on tile t, and P never aliases S.
+// Clusters of CS CTAs (consecutive query tiles of one unit) share every K/V
+// tile: each CTA loads 128/CS of its rows and multicasts them; a stage is
+// refilled only after every CTA of the cluster released it.
 // Every mbarrier wait is bounded; on timeout the CTA records
 // STATEKV_E_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM, exits.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+
 #include "statekv_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -36,35 +59,38 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;   // 1 s per wait
 
 template <int D>
 struct TcLayout {
-    static constexpr int BM = 128, BN = 128;
+    static constexpr int BN = 128;
     static constexpr int KCH = D / 64;                  // 128-byte chunks along d
-    static constexpr int CHUNK = 128 * 128;             // [128 rows][64 bf16]
-    static constexpr int Q_BYTES = KCH * CHUNK;
-    static constexpr int KV_BYTES = KCH * CHUNK;
-    static constexpr int P_BYTES = 2 * CHUNK;           // [128 rows][128 keys]
-    static constexpr int NS = 2;                        // K/V pipeline stages
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-    static constexpr int OFF_P = OFF_V + NS * KV_BYTES;
-    static constexpr int OFF_COL = OFF_P + P_BYTES;     // float [2][4][128]
-    static constexpr int OFF_BAR = OFF_COL + 2 * 4 * 128 * 4;
-    // barriers
-    static constexpr int B_Q = 0;
-    static constexpr int B_KV_FULL = 1;
-    static constexpr int B_KV_EMPTY = B_KV_FULL + NS;
-    static constexpr int B_S_FULL = B_KV_EMPTY + NS;
-    static constexpr int B_S_EMPTY = B_S_FULL + 2;
-    static constexpr int B_P_FULL = B_S_EMPTY + 2;
-    static constexpr int B_P_EMPTY = B_P_FULL + 1;
-    static constexpr int B_O_FULL = B_P_EMPTY + 1;
+    static constexpr int CHUNK = 128 * 128;             // [128 rows][64 bf16], 128B-swizzled
+    static constexpr int TILE = KCH * CHUNK;            // one K or V tile
+    static constexpr int KS = 4, VS = 2;                // K and V pipeline stages
+    static constexpr int SB1 = 3;                       // sweep-1 S buffers
+    static constexpr int NCOL = 3;                      // column-sum exchange slots
+    static constexpr int SW = 16;                       // softmax warps
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + KS * TILE;
+    static constexpr int OFF_COL = OFF_V + VS * TILE;   // float [NCOL][4 quarters][128]
+    static constexpr int OFF_STAT = OFF_COL + NCOL * 4 * 128 * 4;   // float2 [4 chunks][128 rows]
+    static constexpr int OFF_BAR = OFF_STAT + 4 * 128 * 8;
+    static constexpr int B_Q = 0;                       // Q in TMEM (all softmax warps)
+    static constexpr int B_K_FULL = 1;
+    static constexpr int B_K_EMPTY = B_K_FULL + KS;
+    static constexpr int B_V_FULL = B_K_EMPTY + KS;
+    static constexpr int B_V_EMPTY = B_V_FULL + VS;
+    static constexpr int B_S_FULL = B_V_EMPTY + VS;     // [SB1] S buffer computed
+    static constexpr int B_S_READ = B_S_FULL + SB1;     // [SB1] S buffer loaded by all softmax warps
+    static constexpr int B_P_FULL = B_S_READ + SB1;     // [2] P buffer written
+    static constexpr int B_P_FREE = B_P_FULL + 2;       // [2] P buffer consumed by PV
+    static constexpr int B_O_FULL = B_P_FREE + 2;
     static constexpr int B_DRAIN = B_O_FULL + 1;
-    static constexpr int B_COL = B_DRAIN + 1;          // column-sum buffer ready [2]
-    static constexpr int NBAR = B_COL + 2;
+    static constexpr int B_COL = B_DRAIN + 1;           // [NCOL] column-sum exchange
+    static constexpr int B_STAT = B_COL + NCOL;         // row-statistics exchange
+    static constexpr int NBAR = B_STAT + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_O = 256;
+    static constexpr uint32_t TM_O = 128, TM_P = 256, TM_Q = 448;
+    static constexpr int THREADS = 64 + 32 * SW;
 };
 
 struct Sync {
@@ -75,14 +101,17 @@ struct Sync {
     __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 
     // Wait for the phase of the given parity; gives up on abort or timeout.
-    __device__ bool wait(int i, uint32_t parity, uint32_t site) const {
+    // Softmax warps sleep in try_wait; the single-thread producer and MMA
+    // issuer poll (they must react within a few cycles of a phase flip).
+    __device__ bool wait(int i, uint32_t parity, uint32_t site, bool poll = false) const {
         const uint32_t b = bar(i);
-        if (ptx::mbar_test(b, parity)) return true;
+        if (ptx::mbar_poll(b, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
-        for (uint32_t spin = 1;; ++spin) {
-            if (ptx::mbar_test(b, parity)) return true;
+        for (;;) {
+            if (poll ? ptx::mbar_poll(b, parity) : ptx::mbar_wait_hint(b, parity, 20000u))
+                return true;
             if (*abort) return false;
-            if ((spin & 255u) == 0 && globaltimer_ns() - t0 > kTimeoutNs) {
+            if (globaltimer_ns() - t0 > kTimeoutNs) {
                 *abort = 1u;
                 record_error(err, (uint32_t)STATEKV_E_TIMEOUT, site, (uint32_t)i);
                 return false;
@@ -93,7 +122,7 @@ struct Sync {
     __device__ void drain(int i, uint32_t parity) const {
         const uint32_t b = bar(i);
         const uint64_t t0 = globaltimer_ns();
-        while (!ptx::mbar_test(b, parity)) {
+        while (!ptx::mbar_wait_hint(b, parity, 20000u)) {
             if (globaltimer_ns() - t0 > kTimeoutNs) {
                 record_error(err, (uint32_t)STATEKV_E_TIMEOUT, kSiteDrain, (uint32_t)i);
                 return;
@@ -102,29 +131,30 @@ struct Sync {
     }
 };
 
-// Column sums of a 32x32 block held one row per lane: after the call lane l
-// holds the sum over the 32 lanes of column l.  Recursive halving: at each
-// step a lane keeps half of its columns and adds its partner's copy of them.
-__device__ __forceinline__ float warp_column_sum32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-        const bool up = (lane & w) != 0;
-#pragma unroll
-        for (int j = 0; j < w; ++j) {
-            float send = up ? v[j] : v[j + w];
-            float keep = up ? v[j + w] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
-    }
-    return v[0];
+// Key range of one 128-row query tile: tiles [0, nt) hold a key visible to
+// some row; tiles [0, nfull) are visible to every row.
+struct TileRange {
+    int row0, nt, nfull;
+};
+__device__ __forceinline__ TileRange tile_range(int row0, int GT, int T, int c) {
+    TileRange r{row0, 0, 0};
+    if (row0 >= GT) return r;
+    const int r1 = min(row0 + 128, GT) - 1;
+    const bool one_head = (row0 / T) == (r1 / T);
+    const int imax = one_head ? r1 % T : T - 1;
+    const int imin = one_head ? row0 % T : 0;
+    r.nt = (c + imax + 1 + 127) / 128;
+    r.nfull = (c + imin + 1) / 128;
+    return r;
 }
 
-template <int D>
-__global__ void __launch_bounds__(192, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-               const __grid_constant__ CUtensorMap tm_k,
+template <int D, int CS>
+__global__ void __launch_bounds__(TcLayout<D>::THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, AttnArgs a) {
     using L = TcLayout<D>;
+    constexpr int SLICE = 128 / CS;                     // K/V rows loaded by each CTA
+    constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -132,37 +162,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rt = a.n_row_tiles;
-    const int u = blockIdx.x / n_rt;
-    const int mt = blockIdx.x - u * n_rt;
-    const int r0 = mt * L::BM;
-    const int r1 = min(r0 + L::BM, a.GT) - 1;
-    const bool one_head = (r0 / a.T) == (r1 / a.T);
-    const int imax = one_head ? r1 % a.T : a.T - 1;
-    const int imin = one_head ? r0 % a.T : 0;
-    const int nkeys = a.c + imax + 1;                 // keys visible to some row
-    const int nt = (nkeys + L::BN - 1) / L::BN;       // key tiles
-    const int nfull = (a.c + imin + 1) / L::BN;       // tiles visible to every row
+    const int n_slots = (n_rt + CS - 1) / CS * CS;       // row tiles padded to whole clusters
+    const int u = blockIdx.x / n_slots;
+    const int mt = blockIdx.x - u * n_slots;
+    const int rank = CS > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const TileRange me = tile_range(mt * 128, a.GT, a.T, a.c);
+    int nt_load = 0;                                    // key tiles the cluster streams
+    for (int r = 0; r < CS; ++r)
+        nt_load = max(nt_load, tile_range((mt - rank + r) * 128, a.GT, a.T, a.c).nt);
 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + L::OFF_MISC + 4);
     Sync sy{sbase + (uint32_t)L::OFF_BAR, abort_flag, a.err};
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(sy.bar(L::B_Q), 1);
-        for (int s = 0; s < L::NS; ++s) {
-            ptx::mbar_init(sy.bar(L::B_KV_FULL + s), 1);
-            ptx::mbar_init(sy.bar(L::B_KV_EMPTY + s), 1);
+        ptx::mbar_init(sy.bar(L::B_Q), L::SW);
+        for (int s = 0; s < L::KS; ++s) {
+            ptx::mbar_init(sy.bar(L::B_K_FULL + s), 1);
+            ptx::mbar_init(sy.bar(L::B_K_EMPTY + s), CS);   // one release per CTA
+        }
+        for (int s = 0; s < L::VS; ++s) {
+            ptx::mbar_init(sy.bar(L::B_V_FULL + s), 1);
+            ptx::mbar_init(sy.bar(L::B_V_EMPTY + s), CS);
+        }
+        for (int b = 0; b < L::SB1; ++b) {
+            ptx::mbar_init(sy.bar(L::B_S_FULL + b), 1);
+            ptx::mbar_init(sy.bar(L::B_S_READ + b), L::SW);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(sy.bar(L::B_S_FULL + b), 1);
-            ptx::mbar_init(sy.bar(L::B_S_EMPTY + b), 4);
+            ptx::mbar_init(sy.bar(L::B_P_FULL + b), L::SW);
+            ptx::mbar_init(sy.bar(L::B_P_FREE + b), 1);
         }
-        ptx::mbar_init(sy.bar(L::B_P_FULL), 4);
-        ptx::mbar_init(sy.bar(L::B_P_EMPTY), 1);
+        for (int c = 0; c < L::NCOL; ++c) ptx::mbar_init(sy.bar(L::B_COL + c), L::SW);
         ptx::mbar_init(sy.bar(L::B_O_FULL), 1);
         ptx::mbar_init(sy.bar(L::B_DRAIN), 1);
-        ptx::mbar_init(sy.bar(L::B_COL), 4);
-        ptx::mbar_init(sy.bar(L::B_COL + 1), 4);
+        ptx::mbar_init(sy.bar(L::B_STAT), L::SW);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -172,273 +206,527 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     ptx::tc_fence_before();
     __syncthreads();
+    // peers multicast into this CTA's shared memory and barriers: all of
+    // them must be initialised first
+    if (CS > 1) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const uint32_t sQ = sbase + L::OFF_Q;
     const uint32_t sK = sbase + L::OFF_K;
     const uint32_t sV = sbase + L::OFF_V;
-    const uint32_t sP = sbase + L::OFF_P;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            ptx::tma_prefetch_desc(&tm_q);
             ptx::tma_prefetch_desc(&tm_k);
             ptx::tma_prefetch_desc(&tm_v);
-            ptx::mbar_arrive_expect_tx(sy.bar(L::B_Q), L::Q_BYTES);
-            for (int kc = 0; kc < L::KCH; ++kc)
-                ptx::tma_load_3d(sQ + kc * L::CHUNK, &tm_q, sy.bar(L::B_Q), kc * 64, r0, u);
-            int issued_phase[L::NS];
-            for (int s = 0; s < L::NS; ++s) issued_phase[s] = -1;
-            int it = 0;
-            for (int sweep = 0; sweep < 2; ++sweep) {
-                const uint32_t bytes = L::KV_BYTES * (sweep ? 2 : 1);
-                bool ok = true;
-                for (int t = 0; t < nt; ++t, ++it) {
-                    const int s = it % L::NS, js = it / L::NS;
-                    if (!sy.wait(L::B_KV_EMPTY + s, (js & 1) ^ 1, kSiteKvEmpty)) { ok = false; break; }
-                    const uint32_t fb = sy.bar(L::B_KV_FULL + s);
-                    ptx::mbar_arrive_expect_tx(fb, bytes);
-                    for (int kc = 0; kc < L::KCH; ++kc)
-                        ptx::tma_load_3d(sK + s * L::KV_BYTES + kc * L::CHUNK, &tm_k, fb,
-                                         kc * 64, t * L::BN, u);
-                    if (sweep)
-                        for (int kc = 0; kc < L::KCH; ++kc)
-                            ptx::tma_load_3d(sV + s * L::KV_BYTES + kc * L::CHUNK, &tm_v, fb,
-                                             kc * 64, t * L::BN, u);
-                    issued_phase[s] = js & 1;
+            int kt = 0, vt = 0;                        // K and V loads issued
+            bool ok = true;
+            // load number cnt of a ring of ns stages goes to stage cnt % ns
+            // and completes phase cnt / ns of that stage's full barrier
+            auto load = [&](int t, bool is_v) -> bool {
+                const int ns = is_v ? L::VS : L::KS;
+                const int cnt = is_v ? vt : kt;
+                const int s = cnt % ns, j = cnt / ns;
+                const int empty = (is_v ? L::B_V_EMPTY : L::B_K_EMPTY) + s;
+                if (!sy.wait(empty, (uint32_t)(j & 1) ^ 1u, kSiteKvEmpty, true)) return false;
+                const uint32_t fb = sy.bar((is_v ? L::B_V_FULL : L::B_K_FULL) + s);
+                ptx::mbar_arrive_expect_tx(fb, L::TILE);
+                const uint32_t dst = (is_v ? sV : sK) + s * L::TILE + rank * SLICE * 128;
+                const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+#pragma unroll
+                for (int kc = 0; kc < L::KCH; ++kc) {
+                    if (CS > 1)
+                        ptx::tma_load_3d_mc(dst + kc * L::CHUNK, map, fb, kc * 64,
+                                            t * L::BN + rank * SLICE, u, kMask);
+                    else
+                        ptx::tma_load_3d(dst + kc * L::CHUNK, map, fb, kc * 64, t * L::BN, u);
                 }
-                if (!ok) break;
+                if (is_v) ++vt; else ++kt;
+                return true;
+            };
+            // the order of first use: sweep 1 K(0..), sweep 2 K(0) K(1) then
+            // V(t) K(t+2) for every t
+            for (int t = 0; ok && t < nt_load; ++t) ok = load(t, false);
+            for (int t = 0; ok && t < min(2, nt_load); ++t) ok = load(t, false);
+            for (int t = 0; ok && t < nt_load; ++t) {
+                ok = load(t, true);
+                if (ok && t + 2 < nt_load) ok = load(t + 2, false);
             }
-            // never leave a copy in flight into this CTA's shared memory
-            sy.drain(L::B_Q, 0);
-            for (int s = 0; s < L::NS; ++s)
-                if (issued_phase[s] >= 0) sy.drain(L::B_KV_FULL + s, (uint32_t)issued_phase[s]);
+            // never leave a copy in flight into this CTA's shared memory: wait
+            // for the last load of every stage (load n of stage s is number
+            // s + n * stages, its phase parity n & 1)
+            for (int s = 0; s < L::KS && s < kt; ++s)
+                sy.drain(L::B_K_FULL + s, (uint32_t)(((kt - 1 - s) / L::KS) & 1));
+            for (int s = 0; s < L::VS && s < vt; ++s)
+                sy.drain(L::B_V_FULL + s, (uint32_t)(((vt - 1 - s) / L::VS) & 1));
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, false, true);
-            auto issue_qk = [&](uint32_t d_tmem, uint32_t k_stage) {
+        // The whole warp walks the schedule (its values stay warp-uniform);
+        // one elected lane issues each batch of MMAs and their commits.
+        constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, false, true);
+        // descriptors are built once; a K step of 16 bf16 (32 bytes) adds 2
+        // to the start-address field, a 16-key step of V (2048 bytes) adds 128,
+        // a stage (TILE bytes) adds TILE >> 4; in TMEM a K step of Q is 8 columns
+        const uint32_t desc_hi = (uint32_t)(ptx::sdesc_sw128(0, 16, 1024) >> 32);
+        const uint32_t v_hi = (uint32_t)(ptx::sdesc_sw128(0, L::CHUNK, 1024) >> 32);
+        const uint32_t kb0 = (uint32_t)ptx::sdesc_sw128(sK, 16, 1024);
+        const uint32_t vb0 = (uint32_t)ptx::sdesc_sw128(sV, L::CHUNK, 1024);
+        const uint32_t tq = tmem + L::TM_Q;
+        int kt = 0, vt = 0;                            // K and V tiles consumed
+        uint32_t s_used = 0, s_par = 0;                // per S buffer: issued yet / parity of last issue
+        uint32_t pv_par = 0;                           // per P buffer: parity of the next P_FULL phase
+        // buffer b may be overwritten once every softmax warp loaded its tile
+        auto s_free = [&](int b) -> bool {
+            if (!((s_used >> b) & 1u)) return true;
+            if (!sy.wait(L::B_S_READ + b, (s_par >> b) & 1u, kSiteSEmpty, true)) return false;
+            ptx::tc_fence_after();
+            return true;
+        };
+        // a stage is free once every CTA of the cluster is done with it
+        auto release = [&](int bar) {
+            if (CS > 1) ptx::umma_commit_mc(sy.bar(bar), kMask);
+            else ptx::umma_commit(sy.bar(bar));
+        };
+        auto issue_s = [&](int b, bool needed) -> bool {
+            const int s = kt % L::KS, j = kt / L::KS;
+            if (!sy.wait(L::B_K_FULL + s, (uint32_t)(j & 1), kSiteKvFull, true)) return false;
+            ptx::tc_fence_after();
+            if (needed && !s_free(b)) return false;
+            if (ptx::elect_one()) {
+                if (needed) {
+                    const uint32_t d = tmem + 128u * b;
+                    const uint32_t kb = kb0 + (uint32_t)s * (L::TILE >> 4);
 #pragma unroll
-                for (int kc = 0; kc < L::KCH; ++kc)
+                    for (int kc = 0; kc < L::KCH; ++kc)
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        uint64_t ad = ptx::sdesc_sw128(sQ + kc * L::CHUNK + ks * 32, 16, 1024);
-                        uint64_t bd = ptx::sdesc_sw128(k_stage + kc * L::CHUNK + ks * 32, 16, 1024);
-                        ptx::umma_f16_ss(d_tmem, ad, bd, idesc_qk, (kc | ks) ? 1u : 0u);
-                    }
-            };
-            auto issue_pv = [&](int tt) -> bool {
-                if (!sy.wait(L::B_P_FULL, tt & 1, kSitePFull)) return false;
+                        for (int ks = 0; ks < 4; ++ks)
+                            ptx::umma_ts_lh(d, tq + 32u * kc + 8u * ks,
+                                            kb + kc * (L::CHUNK >> 4) + 2 * ks, desc_hi, idesc_qk,
+                                            (kc | ks) ? 1u : 0u);
+                    ptx::umma_commit(sy.bar(L::B_S_FULL + b));
+                }
+                release(L::B_K_EMPTY + s);
+            }
+            __syncwarp();
+            if (needed) {
+                const uint32_t bit = 1u << b;
+                s_par ^= s_used & bit;
+                s_used |= bit;
+            }
+            ++kt;
+            return true;
+        };
+        // Q is in TMEM once every softmax warp has stored its part
+        bool ok = sy.wait(L::B_Q, 0, kSiteQFull, true);
+        ptx::tc_fence_after();
+        // sweep 1: three S buffers in rotation
+        for (int t = 0, b = 0; ok && t < nt_load; ++t, b = (b == L::SB1 - 1) ? 0 : b + 1)
+            ok = issue_s(b, t < me.nt);
+        // sweep 2: S buffer 0; O and P live where buffers 1 and 2 were, so
+        // every sweep-1 buffer must have been read first.  S(t+1) is issued
+        // as soon as S(t) has been loaded, ahead of PV(t).
+        if (ok) ok = s_free(0) && s_free(1) && s_free(2);
+        if (ok && nt_load > 0) ok = issue_s(0, 0 < me.nt);
+        for (int t = 0; ok && t < nt_load; ++t) {
+            if (t + 1 < nt_load && !(ok = issue_s(0, t + 1 < me.nt))) break;
+            const int vs = vt % L::VS, jv = vt / L::VS;
+            if (!(ok = sy.wait(L::B_V_FULL + vs, (uint32_t)(jv & 1), kSiteKvFull, true))) break;
+            const bool mine = t < me.nt;
+            const int pb = t & 1;
+            if (mine) {
+                // P(t) written by every softmax warp
+                if (!(ok = sy.wait(L::B_P_FULL + pb, (pv_par >> pb) & 1u, kSitePFull, true))) break;
                 ptx::tc_fence_after();
-                const int sp = (nt + tt) % L::NS;
-                const uint32_t v_stage = sV + sp * L::KV_BYTES;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    uint64_t ad = ptx::sdesc_sw128(sP + (ks >> 2) * L::CHUNK + (ks & 3) * 32, 16, 1024);
+            }
+            if (ptx::elect_one()) {
+                if (mine) {
+                    const uint32_t p_tmem = tmem + L::TM_P + 64u * pb;
+                    const uint32_t vb = vb0 + (uint32_t)vs * (L::TILE >> 4);
                     // MN-major V: LBO = distance between 64-wide d chunks,
                     // SBO = distance between 8-key row groups
-                    uint64_t bd = ptx::sdesc_sw128(v_stage + ks * 2048, L::CHUNK, 1024);
-                    ptx::umma_f16_ss(tmem + L::TM_O, ad, bd, idesc_pv, (tt | ks) ? 1u : 0u);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        ptx::umma_ts_lh(tmem + L::TM_O, p_tmem + 8u * ks, vb + 128u * ks, v_hi,
+                                        idesc_pv, (t | ks) ? 1u : 0u);
+                    ptx::umma_commit(sy.bar(L::B_P_FREE + pb));
                 }
-                ptx::umma_commit(sy.bar(L::B_P_EMPTY));
-                ptx::umma_commit(sy.bar(L::B_KV_EMPTY + sp));
-                return true;
-            };
-            bool ok = sy.wait(L::B_Q, 0, kSiteQFull);
-            ptx::tc_fence_after();
-            int it = 0;
-            for (int t = 0; ok && t < nt; ++t, ++it) {            // sweep 1
-                const int b = it & 1, jb = it >> 1, s = it % L::NS, js = it / L::NS;
-                if (!sy.wait(L::B_S_EMPTY + b, (jb & 1) ^ 1, kSiteSEmpty)) { ok = false; break; }
-                if (!sy.wait(L::B_KV_FULL + s, js & 1, kSiteKvFull)) { ok = false; break; }
-                ptx::tc_fence_after();
-                issue_qk(tmem + b * 128, sK + s * L::KV_BYTES);
-                ptx::umma_commit(sy.bar(L::B_KV_EMPTY + s));
-                ptx::umma_commit(sy.bar(L::B_S_FULL + b));
+                release(L::B_V_EMPTY + vs);
             }
-            for (int t = 0; ok && t < nt; ++t, ++it) {            // sweep 2
-                const int b = it & 1, jb = it >> 1, s = it % L::NS, js = it / L::NS;
-                if (!sy.wait(L::B_S_EMPTY + b, (jb & 1) ^ 1, kSiteSEmpty)) { ok = false; break; }
-                if (!sy.wait(L::B_KV_FULL + s, js & 1, kSiteKvFull)) { ok = false; break; }
-                ptx::tc_fence_after();
-                issue_qk(tmem + b * 128, sK + s * L::KV_BYTES);
-                ptx::umma_commit(sy.bar(L::B_S_FULL + b));
-                if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
-            }
-            if (ok && nt > 0 && issue_pv(nt - 1)) ptx::umma_commit(sy.bar(L::B_O_FULL));
-            // all MMAs complete before TMEM is released
+            __syncwarp();
+            if (mine) pv_par ^= 1u << pb;
+            ++vt;
+        }
+        // all MMAs complete before TMEM is released (the elected lane is the
+        // lowest active lane every time, so it issued every MMA above)
+        if (ptx::elect_one()) {
+            if (ok) ptx::umma_commit(sy.bar(L::B_O_FULL));
             ptx::umma_commit(sy.bar(L::B_DRAIN));
-            sy.drain(L::B_DRAIN, 0);
         }
+        __syncwarp();
+        sy.drain(L::B_DRAIN, 0);
     } else {
-        // ------------------------------------------------------------ epilogue
-        const int q4 = warp & 3;                      // TMEM lane quarter
-        const int row = q4 * 32 + lane;
-        const int r_unit = r0 + row;
-        const bool valid = r_unit < a.GT;
-        const int lim = valid ? a.c + (r_unit % a.T) : -1;    // kk visible iff kk <= lim
-        const uint32_t t_lane = tmem + ((uint32_t)(q4 * 32) << 16);
-        float* colbuf = reinterpret_cast<float*>(base + L::OFF_COL);
-        float* colsum = a.colsum + ((int64_t)u * n_rt + mt) * a.m_pad;
+        // ------------------------------------------------------------ softmax
+        // thread rows: 32*q4 + 16*hh + lane/4 + 8*sub (ri = 2*hh + sub);
+        // columns of chunk cq: 32*cq + 8*rp + 2*(lane%4) + {0,1}
+        const int sw = warp - 2;
+        const int q4 = warp & 3;                       // TMEM lane quarter
+        const int cq = sw >> 2;                        // 32-column chunk of the tile
         const float sc = a.scale_log2;
-        int it = 0;
+        const uint32_t lane_h0 = (uint32_t)(q4 * 32) << 16;
+        const uint32_t lane_h1 = (uint32_t)(q4 * 32 + 16) << 16;
+        int lim[4];
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri) {
+            const int r_unit = me.row0 + q4 * 32 + 16 * (ri >> 1) + (lane >> 2) + 8 * (ri & 1);
+            lim[ri] = r_unit < a.GT ? a.c + (r_unit % a.T) : -1;  // kk visible iff kk <= lim
+        }
+        const int colb = 32 * cq + 2 * (lane & 3);     // tile column of this thread's pair 0
+        float* colbuf = reinterpret_cast<float*>(base + L::OFF_COL);
+        float2* statbuf = reinterpret_cast<float2*>(base + L::OFF_STAT);
+        float* colsum = a.colsum + ((int64_t)u * n_rt + mt) * a.m_pad;
+        uint32_t s_par = 0;                            // per S buffer: parity of the next S_FULL phase
         bool ok = true;
+        auto load_s = [&](uint32_t t_s, uint32_t (&r0)[16], uint32_t (&r1)[16]) {
+            ptx::tmem_ld_16x256b_x4(t_s + lane_h0 + 32 * cq, r0);
+            ptx::tmem_ld_16x256b_x4(t_s + lane_h1 + 32 * cq, r1);
+            ptx::tmem_ld_wait();
+        };
 
-        // sweep 1: log-sum-exp (log2 domain)
-        float mrun = -INFINITY, lrun = 0.f;
-        for (int t = 0; t < nt; ++t, ++it) {
-            const int b = it & 1, jb = it >> 1;
-            if (!sy.wait(L::B_S_FULL + b, jb & 1, kSiteSFull)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const bool full = t < nfull;
+        // ---- Q -> TMEM: lane = query row, bf16 pairs (even element low) along
+        // the columns; each warp copies its lane quarter's rows, its chunk's
+        // quarter of the d columns.  Rows past the unit's end are zero.
+        {
+            constexpr int QW = D / 8;                  // TMEM columns per chunk warp
+            const int r_unit = me.row0 + q4 * 32 + lane;
+            uint32_t qv[QW];
+            if (r_unit < a.GT) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const uint8_t*>(a.q_rot) + ((int64_t)u * a.GT + r_unit) * (D * 2) +
+                    cq * (D / 2));
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(t_lane + b * 128 + ch * 32, r);
-                ptx::tmem_ld_wait();
-                float x[32];
-                float mx = -INFINITY;
-                const int k0 = t * L::BN + ch * 32;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float v = __uint_as_float(r[j]) * sc;
-                    if (!full && k0 + j > lim) v = -INFINITY;
-                    x[j] = v;
-                    mx = fmaxf(mx, v);
+                for (int j = 0; j < QW / 4; ++j) {
+                    const uint4 v = src[j];
+                    qv[4 * j] = v.x; qv[4 * j + 1] = v.y; qv[4 * j + 2] = v.z; qv[4 * j + 3] = v.w;
                 }
-                const float mn = fmaxf(mrun, mx);
-                if (mn != -INFINITY) {
-                    float sum = 0.f;
+            } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sum += ptx::ex2_approx(x[j] - mn);
-                    lrun = lrun * ptx::ex2_approx(mrun - mn) + sum;
-                    mrun = mn;
-                }
+                for (int j = 0; j < QW; ++j) qv[j] = 0u;
             }
+            const uint32_t t_q = tmem + L::TM_Q + lane_h0 + QW * cq;
+            if constexpr (QW == 16) ptx::tmem_st_32x32b_x16(t_q, qv);
+            else ptx::tmem_st_32x32b_x8(t_q, qv);
+            ptx::tmem_st_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S_EMPTY + b));
+            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_Q));
         }
-        const float lse2 = (valid && lrun > 0.f) ? mrun + log2f(lrun) : INFINITY;
 
-        // sweep 2: P, column sums, P -> shared memory for PV
-        for (int t = 0; ok && t < nt; ++t, ++it) {
-            const int b = it & 1, jb = it >> 1;
-            if (!sy.wait(L::B_S_FULL + b, jb & 1, kSiteSFull)) { ok = false; break; }
+        // ---- sweep 1: per-thread running max / sum of exp2 over its columns
+        float mrow[4], lrow[4];
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri) { mrow[ri] = -INFINITY; lrow[ri] = 0.f; }
+        for (int t = 0, b = 0; t < me.nt; ++t, b = (b == L::SB1 - 1) ? 0 : b + 1) {
+            if (!sy.wait(L::B_S_FULL + b, (s_par >> b) & 1u, kSiteSFull)) { ok = false; break; }
             ptx::tc_fence_after();
-            const bool full = t < nfull;
-            uint32_t pk[4][16];
-            float cval[4];
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(t_lane + b * 128 + ch * 32, r);
-                ptx::tmem_ld_wait();
-                float p[32];
-                const int k0 = t * L::BN + ch * 32;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float e = ptx::ex2_approx(fmaf(__uint_as_float(r[j]), sc, -lse2));
-                    p[j] = (full || k0 + j <= lim) ? e : 0.f;
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(p[2 * j], p[2 * j + 1]);
-                    pk[ch][j] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                cval[ch] = warp_column_sum32(p, lane);
-            }
+            uint32_t r0[16], r1[16];
+            load_s(tmem + 128u * b, r0, r1);
+            // the buffer is free for the next S as soon as it is in registers
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S_EMPTY + b));
-
-            float* cb = colbuf + (t & 1) * 512 + q4 * 128;
+            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S_READ + b));
+            s_par ^= 1u << b;
+            const bool diag = t >= me.nfull;
+            const int k0 = t * L::BN + colb;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) cb[ch * 32 + lane] = cval[ch];
-
-            if (!sy.wait(L::B_P_EMPTY, (t & 1) ^ 1, kSitePEmpty)) { ok = false; break; }
+            for (int ri = 0; ri < 4; ++ri) {
+                const uint32_t* r = (ri >> 1) ? r1 : r0;
+                const int sub = ri & 1;
+                float x[8];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const uint32_t chunk = sP + (ch >> 1) * L::CHUNK + row * 128;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t unit16 = (uint32_t)((ch & 1) * 4 + w);
-                    const uint32_t addr = chunk + ((unit16 ^ (uint32_t)(row & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 :: "r"(addr), "r"(pk[ch][4 * w]), "r"(pk[ch][4 * w + 1]),
-                                    "r"(pk[ch][4 * w + 2]), "r"(pk[ch][4 * w + 3]) : "memory");
+                for (int rp = 0; rp < 4; ++rp) {
+                    x[2 * rp] = __uint_as_float(r[4 * rp + 2 * sub]);
+                    x[2 * rp + 1] = __uint_as_float(r[4 * rp + 2 * sub + 1]);
                 }
+                if (diag) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (k0 + 8 * (e >> 1) + (e & 1) > lim[ri]) x[e] = -INFINITY;
+                }
+                const float mx = ptx::max3(ptx::max3(x[0], x[1], x[2]),
+                                           ptx::max3(x[3], x[4], x[5]),
+                                           ptx::max3(x[6], x[7], mrow[ri]));
+                // branch-free online update; -inf rows stay at l = 0
+                const float nms = (mx == -INFINITY) ? 0.f : -mx * sc;
+                const float f = ptx::ex2_approx(fmaf(mrow[ri], sc, nms));
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    float2 z = ptx::fma2(make_float2(x[e], x[e + 1]), make_float2(sc, sc),
+                                         make_float2(nms, nms));
+                    acc = ptx::add2(acc, make_float2(ptx::ex2_approx(z.x), ptx::ex2_approx(z.y)));
+                }
+                lrow[ri] = fmaf(lrow[ri], f, acc.x + acc.y);
+                mrow[ri] = mx;
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_P_FULL));
-
-            // all four warps' partial column sums of this tile are in smem
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_COL + (t & 1)));
-            if (!sy.wait(L::B_COL + (t & 1), (t >> 1) & 1, kSiteCol)) { ok = false; break; }
-            const int e = q4 * 32 + lane;
-            const float* cb0 = colbuf + (t & 1) * 512;
-            colsum[t * L::BN + e] = cb0[e] + cb0[128 + e] + cb0[256 + e] + cb0[384 + e];
         }
-        for (int kk = nt * L::BN + row; kk < a.m_pad; kk += 128) colsum[kk] = 0.f;
+        // combine: the 4 lanes of a row (bits 0, 1), then the 4 chunk warps
+        auto merge = [&](float& m, float& l, float m2, float l2) {
+            const float mn = fmaxf(m, m2);
+            if (mn != -INFINITY) {
+                const float f1 = (m == -INFINITY) ? 0.f : ptx::ex2_approx((m - mn) * sc);
+                const float f2 = (m2 == -INFINITY) ? 0.f : ptx::ex2_approx((m2 - mn) * sc);
+                l = l * f1 + l2 * f2;
+            }
+            m = mn;
+        };
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri)
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, mrow[ri], off);
+                const float l2 = __shfl_xor_sync(0xffffffffu, lrow[ri], off);
+                merge(mrow[ri], lrow[ri], m2, l2);
+            }
+        if ((lane & 3) == 0) {
+#pragma unroll
+            for (int ri = 0; ri < 4; ++ri) {
+                const int row = q4 * 32 + 16 * (ri >> 1) + (lane >> 2) + 8 * (ri & 1);
+                statbuf[cq * 128 + row] = make_float2(mrow[ri], lrow[ri]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_STAT));
+        float lse2[4];
+        if (!sy.wait(L::B_STAT, 0, kSiteCol)) ok = false;
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri) {
+            const int row = q4 * 32 + 16 * (ri >> 1) + (lane >> 2) + 8 * (ri & 1);
+            float m = -INFINITY, l = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 st = statbuf[j * 128 + row];
+                merge(m, l, st.x, st.y);
+            }
+            lse2[ri] = (lim[ri] >= 0 && l > 0.f) ? fmaf(m, sc, log2f(l)) : INFINITY;
+        }
 
-        // output rows
-        if (ok && sy.wait(L::B_O_FULL, 0, kSiteOFull)) {
+        // ---- sweep 2: P, its column sums, P -> TMEM (bf16) for PV
+        uint32_t p_used = 0, p_par = 0;                // per P buffer: written yet / parity of last write
+        // column sums of tile t are summed over the 4 lane quarters during
+        // tile t+1 (by warps 0..3), from slot t % NCOL of the exchange buffer
+        auto finish_col = [&](int t, int slot) -> bool {
+            if (!sy.wait(L::B_COL + slot, (uint32_t)((t / L::NCOL) & 1), kSiteCol)) return false;
+            const int e = sw * 32 + lane;
+            const float* cb = colbuf + slot * 512 + e;
+            colsum[t * L::BN + e] = cb[0] + cb[128] + cb[256] + cb[384];
+            return true;
+        };
+        for (int t = 0, slot = 0; ok && t < me.nt; ++t, slot = (slot == L::NCOL - 1) ? 0 : slot + 1) {
+            constexpr int b = 0;
+            if (!sy.wait(L::B_S_FULL + b, (s_par >> b) & 1u, kSiteSFull)) { ok = false; break; }
             ptx::tc_fence_after();
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) + ((int64_t)u * a.GT + r_unit) * D;
+            uint32_t r0[16], r1[16];
+            load_s(tmem + 128u * b, r0, r1);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S_READ + b));
+            s_par ^= 1u << b;
+            const bool diag = t >= me.nfull;
+            const int k0 = t * L::BN + colb;
+            float c[8];                                // column partials: k = 2*rp + e
+            uint32_t pk[2][8];
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(t_lane + L::TM_O + ch * 32, r);
-                ptx::tmem_ld_wait();
-                if (valid) {
-                    uint32_t w[16];
+            for (int ri = 0; ri < 4; ++ri) {
+                const uint32_t* r = (ri >> 1) ? r1 : r0;
+                const int sub = ri & 1;
+                const float nl = -lse2[ri];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]),
-                                                                 __uint_as_float(r[2 * j + 1]));
-                        w[j] = *reinterpret_cast<uint32_t*>(&h);
+                for (int rp = 0; rp < 4; ++rp) {
+                    float2 z = ptx::fma2(make_float2(__uint_as_float(r[4 * rp + 2 * sub]),
+                                                     __uint_as_float(r[4 * rp + 2 * sub + 1])),
+                                         make_float2(sc, sc), make_float2(nl, nl));
+                    float2 p = make_float2(ptx::ex2_approx(z.x), ptx::ex2_approx(z.y));
+                    if (diag) {
+                        if (k0 + 8 * rp > lim[ri]) p.x = 0.f;
+                        if (k0 + 8 * rp + 1 > lim[ri]) p.y = 0.f;
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                    if (ri == 0) { c[2 * rp] = p.x; c[2 * rp + 1] = p.y; }
+                    else {
+                        const float2 cc = ptx::add2(make_float2(c[2 * rp], c[2 * rp + 1]), p);
+                        c[2 * rp] = cc.x; c[2 * rp + 1] = cc.y;
+                    }
+                    pk[ri >> 1][2 * rp + sub] = ptx::pack_bf16x2(p.x, p.y);
                 }
+            }
+            // P buffer t&1 is free once PV(t-2) has completed
+            const int pb = t & 1;
+            if (((p_used >> pb) & 1u) && !sy.wait(L::B_P_FREE + pb, (p_par >> pb) & 1u, kSitePEmpty)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t t_p = tmem + L::TM_P + 64u * pb + 16u * cq;
+            ptx::tmem_st_16x128b_x4(t_p + lane_h0, pk[0]);
+            ptx::tmem_st_16x128b_x4(t_p + lane_h1, pk[1]);
+            // column sums over the warp's 32 rows: lanes sharing lane&3 hold the
+            // same columns; reduce over lane bits 4, 3, 2 (keep half each)
+#pragma unroll
+            for (int half = 4, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+                const bool up = (lane & bit) != 0;
+#pragma unroll
+                for (int j = 0; j < half; ++j) {
+                    const float send = up ? c[j] : c[j + half];
+                    const float keep = up ? c[j + half] : c[j];
+                    c[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+                }
+            }
+            // lane holds chunk column 8*((lane>>3)&3) + 2*(lane&3) + ((lane>>2)&1)
+            // (slot t % NCOL is rewritten at tile t + NCOL, which cannot start
+            // before every warp has loaded S(t+1), i.e. finished tile t)
+            colbuf[slot * 512 + q4 * 128 + 32 * cq + 8 * ((lane >> 3) & 3) + 2 * (lane & 3) +
+                   ((lane >> 2) & 1)] = c[0];
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(sy.bar(L::B_P_FULL + pb));
+                ptx::mbar_arrive(sy.bar(L::B_COL + slot));
+            }
+            p_par ^= p_used & (1u << pb);
+            p_used |= 1u << pb;
+            if (sw < 4 && t > 0 && !finish_col(t - 1, slot == 0 ? L::NCOL - 1 : slot - 1)) {
+                ok = false;
+                break;
+            }
+        }
+        if (ok && sw < 4 && me.nt > 0) ok = finish_col(me.nt - 1, (me.nt - 1) % L::NCOL);
+        if (me.nt > 0)
+            for (int kk = me.nt * L::BN + sw * 32 + lane; kk < a.m_pad; kk += 32 * L::SW)
+                colsum[kk] = 0.f;
+
+        // ---- output rows: quarter q4, 32 columns per warp
+        if (me.nt > 0 && ok && cq < D / 32 && sy.wait(L::B_O_FULL, 0, kSiteOFull)) {
+            ptx::tc_fence_after();
+            const int r_unit = me.row0 + q4 * 32 + lane;
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(tmem + L::TM_O + lane_h0 + 32 * cq, r);
+            ptx::tmem_ld_wait();
+            if (r_unit < a.GT) {
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                     ((int64_t)u * a.GT + r_unit) * D + 32 * cq;
+                uint32_t wv[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    wv[j] = ptx::pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    dst[v4] = make_uint4(wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
             }
         }
         ptx::tc_fence_before();
     }
 
     __syncthreads();
+    // no CTA leaves while a peer may still multicast into it or arrive on
+    // its barriers (every role above has drained its own traffic)
+    if (CS > 1) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, L::TMEM_COLS);
     }
 }
 
-template <int D>
-cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k,
-                      const CUtensorMap& v, cudaStream_t st) {
+template <int D, int CS>
+cudaError_t launch_tc(const AttnArgs& a, const TcMaps& m, cudaStream_t st) {
     using L = TcLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, CS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<D><<<(unsigned)(a.U * a.n_row_tiles), 192, L::SMEM, st>>>(q, k, v, a);
-    return cudaGetLastError();
+    const int n_slots = (a.n_row_tiles + CS - 1) / CS * CS;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.U * n_slots));
+    cfg.blockDim = dim3(L::THREADS);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, CS>, m.k, m.v, a);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 view [units][rows][d] read in boxes of 64 columns (one 128-byte
+// swizzle row) x box_rows rows.
+bool encode_view(CUtensorMap* m, const void* base, int d, int64_t rows, int64_t units,
+                 int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)units};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 }  // namespace
 
-cudaError_t launch_attention_tc(const AttnArgs& a, const CUtensorMap& tm_q,
-                                const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                cudaStream_t st) {
-    if (a.d == 128) return launch_tc<128>(a, tm_q, tm_k, tm_v, st);
-    if (a.d == 64) return launch_tc<64>(a, tm_q, tm_k, tm_v, st);
+int tc_cluster_size(int n_row_tiles) {
+    // CTAs of a cluster are consecutive query tiles of one unit.  Sharing
+    // K/V tiles by multicast cuts L2 reads by the cluster size but couples
+    // the CTAs' pipelines; on GB300 one CTA per tile measured fastest, so
+    // clusters are opt-in (STATEKV_ATTN_CLUSTER = 2 or 4, read when the
+    // tensor maps are built).
+    int want = 1;
+    if (const char* e = getenv("STATEKV_ATTN_CLUSTER")) {
+        const int v = atoi(e);
+        if (v == 2 || v == 4) want = v;
+    }
+    while (want > 1 && n_row_tiles < want) want >>= 1;
+    return want;
+}
+
+bool make_tc_maps(TcMaps* m, const void* pool_k, const void* pool_v, int d, int64_t slots,
+                  int64_t units, int n_row_tiles) {
+    m->cs = tc_cluster_size(n_row_tiles);
+    const int kv_rows = 128 / m->cs;
+    return encode_view(&m->k, pool_k, d, slots, units, kv_rows) &&
+           encode_view(&m->v, pool_v, d, slots, units, kv_rows);
+}
+
+cudaError_t launch_attention_tc(const AttnArgs& a, const TcMaps& m, cudaStream_t st) {
+    if (a.d == 128) {
+        if (m.cs == 4) return launch_tc<128, 4>(a, m, st);
+        if (m.cs == 2) return launch_tc<128, 2>(a, m, st);
+        return launch_tc<128, 1>(a, m, st);
+    }
+    if (a.d == 64) {
+        if (m.cs == 4) return launch_tc<64, 4>(a, m, st);
+        if (m.cs == 2) return launch_tc<64, 2>(a, m, st);
+        return launch_tc<64, 1>(a, m, st);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -13,8 +13,6 @@
 //   Q'         [U*G*T][d]       rotated queries (scratch)
 //   colsum     [U][tiles][m_pad] per query-tile column sums of P
 //   scores     [U][m_pad], score_pos [U][m_pad]
-#include <cudaTypedefs.h>
-
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -44,34 +42,6 @@ struct DeviceGuard {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 3-D bf16 view [units][rows][d] with a 64 x 128 x 1 box and 128-byte swizzle
-// (the box's inner extent is exactly one 128-byte swizzle row).
-bool make_tile_map(CUtensorMap* m, void* base, int d, int64_t rows, int64_t units) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)units};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 struct statekv_handle {
@@ -93,7 +63,7 @@ struct statekv_handle {
     int32_t* score_pos = nullptr;
     uint32_t* err = nullptr;            // device status word
     void* stage_q = nullptr; void* stage_k = nullptr; void* stage_v = nullptr; void* stage_o = nullptr;
-    CUtensorMap tm_q{}, tm_k{}, tm_v{};
+    TcMaps tc{};                        // TMA views for the bf16 attention kernel
 
     bool profiling = false;
     std::vector<PendingEvent> pending;
@@ -234,7 +204,7 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     aa.m_pad = h->m_pad; aa.n_row_tiles = h->n_row_tiles;
     aa.scale = h->scale; aa.scale_log2 = h->scale_log2;
     e = timed(h, STATEKV_KERNEL_ATTENTION, st, [&] {
-        return c.dtype == STATEKV_BF16 ? launch_attention_tc(aa, h->tm_q, h->tm_k, h->tm_v, st)
+        return c.dtype == STATEKV_BF16 ? launch_attention_tc(aa, h->tc, st)
                                        : launch_attention_simt(aa, st);
     });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
@@ -326,12 +296,9 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
         cudaSuccess) {
         free_all(h); delete h; return STATEKV_E_CUDA;
     }
-    if (c.dtype == STATEKV_BF16) {
-        if (!make_tile_map(&h->tm_q, h->q_rot, d, h->GT, h->U) ||
-            !make_tile_map(&h->tm_k, h->pool_k, d, h->slots, h->U) ||
-            !make_tile_map(&h->tm_v, h->pool_v, d, h->slots, h->U)) {
-            free_all(h); delete h; return STATEKV_E_CUDA;
-        }
+    if (c.dtype == STATEKV_BF16 &&
+        !make_tc_maps(&h->tc, h->pool_k, h->pool_v, d, h->slots, h->U, h->n_row_tiles)) {
+        free_all(h); delete h; return STATEKV_E_CUDA;
     }
     if (cudaDeviceSynchronize() != cudaSuccess) { free_all(h); delete h; return STATEKV_E_CUDA; }
     *out = h;
