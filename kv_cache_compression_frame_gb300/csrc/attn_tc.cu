@@ -21,12 +21,13 @@
 //            O += P V (tcgen05 with A in TMEM, V read MN-major from shared
 //            memory).  P is normalised before PV, so O needs no rescaling.
 //
-// Warp roles (576 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// single-thread MMA issuer, warps 2..17 softmax.  Softmax warp w covers TMEM
-// lane quarter w % 4 (the only lanes it may access) and 32-column chunk
-// (w - 2) / 4 of every S tile; with the 16x256b load shape a thread holds
-// 4 rows x 8 columns, so row statistics combine across 4 lanes (then across
-// the 4 chunk warps once per sweep) and column sums need a 3-level shuffle
+// Warp roles (608 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// issuer of the S = Q K^T MMAs, warp 2 issuer of the O += P V MMAs, warps
+// 3..18 softmax.  Softmax warp w covers TMEM lane quarter w % 4 (the only
+// lanes it may access) and 32-column chunk (w - 3) / 4 of every S tile;
+// with the 16x256b load shape a thread holds 4 rows x 8 columns, so row
+// statistics combine across 4 lanes (then across the 4 chunk warps once per
+// sweep) and column sums need a 3-level shuffle
 // reduction (then across the 4 lane quarters in shared memory, one tile
 // behind, so no warp waits for the others within a tile).
 // Shared-memory bandwidth (128 B/clk/SM) is the scarce resource: an MMA with
@@ -36,10 +37,12 @@
 // TMEM (S = Q K^T: Q; O += P V: P) and only K or V from shared memory, which
 // halves the MMA's share of the bandwidth.
 // TMEM (512 columns): Q (bf16 pairs) at 448..; sweep 1 -- three S buffers
-// (0, 128, 256); sweep 2 -- one S buffer (0..127), O (128..), P double buffer
-// (256..383, bf16 pairs).  An S buffer is handed back to the MMA issuer as
-// soon as its tile has been loaded into registers, so S(t+1) is computed
-// while the softmax works on tile t, and P never aliases S.
+// (0, 128, 256); sweep 2 -- two S buffers (0, 128), O (256..), P (384..447,
+// bf16 pairs).  An S buffer is handed back to the MMA issuer as soon as its
+// tile has been loaded into registers, so S(t+1) is computed while the
+// softmax works on S(t) and never waits for the signal that S(t) was read
+// (that arrive sits in the same per-SMSP queue as the softmax's ex2 burst
+// and completes late); P never aliases S.
 // Clusters of CS CTAs (consecutive query tiles of one unit) share every K/V
 // tile: each CTA loads 128/CS of its rows and multicasts them; a stage is
 // refilled only after every CTA of the cluster released it.
@@ -79,18 +82,18 @@ struct TcLayout {
     static constexpr int B_V_EMPTY = B_V_FULL + VS;
     static constexpr int B_S_FULL = B_V_EMPTY + VS;     // [SB1] S buffer computed
     static constexpr int B_S_READ = B_S_FULL + SB1;     // [SB1] S buffer loaded by all softmax warps
-    static constexpr int B_P_FULL = B_S_READ + SB1;     // [2] P buffer written
-    static constexpr int B_P_FREE = B_P_FULL + 2;       // [2] P buffer consumed by PV
-    static constexpr int B_O_FULL = B_P_FREE + 2;
-    static constexpr int B_DRAIN = B_O_FULL + 1;
-    static constexpr int B_COL = B_DRAIN + 1;           // [NCOL] column-sum exchange
+    static constexpr int B_P_FULL = B_S_READ + SB1;     // P written by all softmax warps
+    static constexpr int B_P_FREE = B_P_FULL + 1;       // P consumed by PV
+    static constexpr int B_O_FULL = B_P_FREE + 1;
+    static constexpr int B_DRAIN = B_O_FULL + 1;        // [2] each MMA issuer's teardown
+    static constexpr int B_COL = B_DRAIN + 2;           // [NCOL] column-sum exchange
     static constexpr int B_STAT = B_COL + NCOL;         // row-statistics exchange
     static constexpr int NBAR = B_STAT + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_O = 128, TM_P = 256, TM_Q = 448;
-    static constexpr int THREADS = 64 + 32 * SW;
+    static constexpr uint32_t TM_O = 256, TM_P = 384, TM_Q = 448;
+    static constexpr int THREADS = 96 + 32 * SW;
 };
 
 struct Sync {
@@ -101,15 +104,15 @@ struct Sync {
     __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 
     // Wait for the phase of the given parity; gives up on abort or timeout.
-    // Softmax warps sleep in try_wait; the single-thread producer and MMA
-    // issuer poll (they must react within a few cycles of a phase flip).
-    __device__ bool wait(int i, uint32_t parity, uint32_t site, bool poll = false) const {
+    // After one non-blocking probe the thread sleeps in try_wait, which
+    // returns as soon as the phase completes (a spin that also reads the
+    // global timer reacts hundreds of cycles late).
+    __device__ bool wait(int i, uint32_t parity, uint32_t site) const {
         const uint32_t b = bar(i);
         if (ptx::mbar_poll(b, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
-            if (poll ? ptx::mbar_poll(b, parity) : ptx::mbar_wait_hint(b, parity, 20000u))
-                return true;
+            if (ptx::mbar_wait_hint(b, parity, 20000u)) return true;
             if (*abort) return false;
             if (globaltimer_ns() - t0 > kTimeoutNs) {
                 *abort = 1u;
@@ -189,13 +192,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             ptx::mbar_init(sy.bar(L::B_S_FULL + b), 1);
             ptx::mbar_init(sy.bar(L::B_S_READ + b), L::SW);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(sy.bar(L::B_P_FULL + b), L::SW);
-            ptx::mbar_init(sy.bar(L::B_P_FREE + b), 1);
-        }
+        ptx::mbar_init(sy.bar(L::B_P_FULL), L::SW);
+        ptx::mbar_init(sy.bar(L::B_P_FREE), 1);
         for (int c = 0; c < L::NCOL; ++c) ptx::mbar_init(sy.bar(L::B_COL + c), L::SW);
         ptx::mbar_init(sy.bar(L::B_O_FULL), 1);
         ptx::mbar_init(sy.bar(L::B_DRAIN), 1);
+        ptx::mbar_init(sy.bar(L::B_DRAIN + 1), 1);
         ptx::mbar_init(sy.bar(L::B_STAT), L::SW);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
@@ -229,7 +231,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 const int cnt = is_v ? vt : kt;
                 const int s = cnt % ns, j = cnt / ns;
                 const int empty = (is_v ? L::B_V_EMPTY : L::B_K_EMPTY) + s;
-                if (!sy.wait(empty, (uint32_t)(j & 1) ^ 1u, kSiteKvEmpty, true)) return false;
+                if (!sy.wait(empty, (uint32_t)(j & 1) ^ 1u, kSiteKvEmpty)) return false;
                 const uint32_t fb = sy.bar((is_v ? L::B_V_FULL : L::B_K_FULL) + s);
                 ptx::mbar_arrive_expect_tx(fb, L::TILE);
                 const uint32_t dst = (is_v ? sV : sK) + s * L::TILE + rank * SLICE * 128;
@@ -262,37 +264,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 sy.drain(L::B_V_FULL + s, (uint32_t)(((vt - 1 - s) / L::VS) & 1));
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+        // ------------------------------------------------------- S = Q K^T issuer
         // The whole warp walks the schedule (its values stay warp-uniform);
-        // one elected lane issues each batch of MMAs and their commits.
+        // one elected lane issues each batch of MMAs and their commits.  The
+        // PV products have an issuer of their own (warp 2): an issuing thread
+        // stalls while the tensor pipe's queue is full, and S(t+1) must not
+        // wait behind PV(t-1), which waits for the softmax.
         constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false, false);
-        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, false, true);
         // descriptors are built once; a K step of 16 bf16 (32 bytes) adds 2
-        // to the start-address field, a 16-key step of V (2048 bytes) adds 128,
-        // a stage (TILE bytes) adds TILE >> 4; in TMEM a K step of Q is 8 columns
+        // to the start-address field, a stage (TILE bytes) adds TILE >> 4; in
+        // TMEM a K step of Q is 8 columns
         const uint32_t desc_hi = (uint32_t)(ptx::sdesc_sw128(0, 16, 1024) >> 32);
-        const uint32_t v_hi = (uint32_t)(ptx::sdesc_sw128(0, L::CHUNK, 1024) >> 32);
         const uint32_t kb0 = (uint32_t)ptx::sdesc_sw128(sK, 16, 1024);
-        const uint32_t vb0 = (uint32_t)ptx::sdesc_sw128(sV, L::CHUNK, 1024);
         const uint32_t tq = tmem + L::TM_Q;
-        int kt = 0, vt = 0;                            // K and V tiles consumed
+        int kt = 0;                                    // K tiles consumed
         uint32_t s_used = 0, s_par = 0;                // per S buffer: issued yet / parity of last issue
-        uint32_t pv_par = 0;                           // per P buffer: parity of the next P_FULL phase
         // buffer b may be overwritten once every softmax warp loaded its tile
         auto s_free = [&](int b) -> bool {
             if (!((s_used >> b) & 1u)) return true;
-            if (!sy.wait(L::B_S_READ + b, (s_par >> b) & 1u, kSiteSEmpty, true)) return false;
+            if (!sy.wait(L::B_S_READ + b, (s_par >> b) & 1u, kSiteSEmpty)) return false;
             ptx::tc_fence_after();
             return true;
         };
-        // a stage is free once every CTA of the cluster is done with it
-        auto release = [&](int bar) {
-            if (CS > 1) ptx::umma_commit_mc(sy.bar(bar), kMask);
-            else ptx::umma_commit(sy.bar(bar));
-        };
         auto issue_s = [&](int b, bool needed) -> bool {
             const int s = kt % L::KS, j = kt / L::KS;
-            if (!sy.wait(L::B_K_FULL + s, (uint32_t)(j & 1), kSiteKvFull, true)) return false;
+            if (!sy.wait(L::B_K_FULL + s, (uint32_t)(j & 1), kSiteKvFull)) return false;
             ptx::tc_fence_after();
             if (needed && !s_free(b)) return false;
             if (ptx::elect_one()) {
@@ -308,7 +304,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                             (kc | ks) ? 1u : 0u);
                     ptx::umma_commit(sy.bar(L::B_S_FULL + b));
                 }
-                release(L::B_K_EMPTY + s);
+                // the stage is free once every CTA of the cluster is done with it
+                if (CS > 1) ptx::umma_commit_mc(sy.bar(L::B_K_EMPTY + s), kMask);
+                else ptx::umma_commit(sy.bar(L::B_K_EMPTY + s));
             }
             __syncwarp();
             if (needed) {
@@ -320,30 +318,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             return true;
         };
         // Q is in TMEM once every softmax warp has stored its part
-        bool ok = sy.wait(L::B_Q, 0, kSiteQFull, true);
+        bool ok = sy.wait(L::B_Q, 0, kSiteQFull);
         ptx::tc_fence_after();
         // sweep 1: three S buffers in rotation
         for (int t = 0, b = 0; ok && t < nt_load; ++t, b = (b == L::SB1 - 1) ? 0 : b + 1)
             ok = issue_s(b, t < me.nt);
-        // sweep 2: S buffer 0; O and P live where buffers 1 and 2 were, so
-        // every sweep-1 buffer must have been read first.  S(t+1) is issued
-        // as soon as S(t) has been loaded, ahead of PV(t).
-        if (ok) ok = s_free(0) && s_free(1) && s_free(2);
-        if (ok && nt_load > 0) ok = issue_s(0, 0 < me.nt);
+        // sweep 2: S buffers 0 and 1; S(t+1) waits only for S(t-1) to have
+        // been loaded, so it is computed while the softmax works on S(t)
+        if (ok) ok = s_free(0) && s_free(1);
+        for (int t = 0; ok && t < nt_load; ++t) ok = issue_s(t & 1, t < me.nt);
+        // all MMAs complete before TMEM is released
+        if (ptx::elect_one()) ptx::umma_commit(sy.bar(L::B_DRAIN));
+        __syncwarp();
+        sy.drain(L::B_DRAIN, 0);
+    } else if (warp == 2) {
+        // ---------------------------------------------------------- O += P V issuer
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, false, true);
+        // a 16-key step of V (2048 bytes) adds 128 to the start-address field
+        const uint32_t v_hi = (uint32_t)(ptx::sdesc_sw128(0, L::CHUNK, 1024) >> 32);
+        const uint32_t vb0 = (uint32_t)ptx::sdesc_sw128(sV, L::CHUNK, 1024);
+        uint32_t pv_par = 0;                           // parity of the next P_FULL phase
+        bool ok = true;
+        // O overlays sweep-1 S buffer 2: P(0) is written only after every
+        // softmax warp finished sweep 1, so PV(0) waiting for P(0) is enough
         for (int t = 0; ok && t < nt_load; ++t) {
-            if (t + 1 < nt_load && !(ok = issue_s(0, t + 1 < me.nt))) break;
-            const int vs = vt % L::VS, jv = vt / L::VS;
-            if (!(ok = sy.wait(L::B_V_FULL + vs, (uint32_t)(jv & 1), kSiteKvFull, true))) break;
+            const int vs = t % L::VS, jv = t / L::VS;
+            if (!(ok = sy.wait(L::B_V_FULL + vs, (uint32_t)(jv & 1), kSiteKvFull))) break;
             const bool mine = t < me.nt;
-            const int pb = t & 1;
             if (mine) {
                 // P(t) written by every softmax warp
-                if (!(ok = sy.wait(L::B_P_FULL + pb, (pv_par >> pb) & 1u, kSitePFull, true))) break;
+                if (!(ok = sy.wait(L::B_P_FULL, pv_par, kSitePFull))) break;
                 ptx::tc_fence_after();
             }
             if (ptx::elect_one()) {
                 if (mine) {
-                    const uint32_t p_tmem = tmem + L::TM_P + 64u * pb;
+                    const uint32_t p_tmem = tmem + L::TM_P;
                     const uint32_t vb = vb0 + (uint32_t)vs * (L::TILE >> 4);
                     // MN-major V: LBO = distance between 64-wide d chunks,
                     // SBO = distance between 8-key row groups
@@ -351,27 +360,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     for (int ks = 0; ks < 8; ++ks)
                         ptx::umma_ts_lh(tmem + L::TM_O, p_tmem + 8u * ks, vb + 128u * ks, v_hi,
                                         idesc_pv, (t | ks) ? 1u : 0u);
-                    ptx::umma_commit(sy.bar(L::B_P_FREE + pb));
+                    ptx::umma_commit(sy.bar(L::B_P_FREE));
                 }
-                release(L::B_V_EMPTY + vs);
+                if (CS > 1) ptx::umma_commit_mc(sy.bar(L::B_V_EMPTY + vs), kMask);
+                else ptx::umma_commit(sy.bar(L::B_V_EMPTY + vs));
             }
             __syncwarp();
-            if (mine) pv_par ^= 1u << pb;
-            ++vt;
+            if (mine) pv_par ^= 1u;
         }
-        // all MMAs complete before TMEM is released (the elected lane is the
-        // lowest active lane every time, so it issued every MMA above)
         if (ptx::elect_one()) {
             if (ok) ptx::umma_commit(sy.bar(L::B_O_FULL));
-            ptx::umma_commit(sy.bar(L::B_DRAIN));
+            ptx::umma_commit(sy.bar(L::B_DRAIN + 1));
         }
         __syncwarp();
-        sy.drain(L::B_DRAIN, 0);
+        sy.drain(L::B_DRAIN + 1, 0);
     } else {
         // ------------------------------------------------------------ softmax
         // thread rows: 32*q4 + 16*hh + lane/4 + 8*sub (ri = 2*hh + sub);
         // columns of chunk cq: 32*cq + 8*rp + 2*(lane%4) + {0,1}
-        const int sw = warp - 2;
+        const int sw = warp - 3;
         const int q4 = warp & 3;                       // TMEM lane quarter
         const int cq = sw >> 2;                        // 32-column chunk of the tile
         const float sc = a.scale_log2;
@@ -434,9 +441,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             uint32_t r0[16], r1[16];
             load_s(tmem + 128u * b, r0, r1);
             // the buffer is free for the next S as soon as it is in registers
+            // (wait::ld above; the arrive orders no memory access, so it is
+            // relaxed and does not wait for this warp's column-sum stores)
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S_READ + b));
+            if (lane == 0) ptx::mbar_arrive_relaxed(sy.bar(L::B_S_READ + b));
             s_par ^= 1u << b;
             const bool diag = t >= me.nfull;
             const int k0 = t * L::BN + colb;
@@ -514,7 +523,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
 
         // ---- sweep 2: P, its column sums, P -> TMEM (bf16) for PV
-        uint32_t p_used = 0, p_par = 0;                // per P buffer: written yet / parity of last write
+        uint32_t p_par = 0;                            // parity of the P_FREE phase of PV(t-1)
         // column sums of tile t are summed over the 4 lane quarters during
         // tile t+1 (by warps 0..3), from slot t % NCOL of the exchange buffer
         auto finish_col = [&](int t, int slot) -> bool {
@@ -525,14 +534,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             return true;
         };
         for (int t = 0, slot = 0; ok && t < me.nt; ++t, slot = (slot == L::NCOL - 1) ? 0 : slot + 1) {
-            constexpr int b = 0;
+            const int b = t & 1;
             if (!sy.wait(L::B_S_FULL + b, (s_par >> b) & 1u, kSiteSFull)) { ok = false; break; }
             ptx::tc_fence_after();
             uint32_t r0[16], r1[16];
             load_s(tmem + 128u * b, r0, r1);
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S_READ + b));
+            if (lane == 0) ptx::mbar_arrive_relaxed(sy.bar(L::B_S_READ + b));
             s_par ^= 1u << b;
             const bool diag = t >= me.nfull;
             const int k0 = t * L::BN + colb;
@@ -561,14 +570,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     pk[ri >> 1][2 * rp + sub] = ptx::pack_bf16x2(p.x, p.y);
                 }
             }
-            // P buffer t&1 is free once PV(t-2) has completed
-            const int pb = t & 1;
-            if (((p_used >> pb) & 1u) && !sy.wait(L::B_P_FREE + pb, (p_par >> pb) & 1u, kSitePEmpty)) {
+            // P is free once PV(t-1) has completed (it was issued when P(t-1)
+            // was complete, about one tile of softmax work ago)
+            if (t > 0 && !sy.wait(L::B_P_FREE, p_par, kSitePEmpty)) {
                 ok = false;
                 break;
             }
+            if (t > 0) p_par ^= 1u;
             ptx::tc_fence_after();
-            const uint32_t t_p = tmem + L::TM_P + 64u * pb + 16u * cq;
+            const uint32_t t_p = tmem + L::TM_P + 16u * cq;
             ptx::tmem_st_16x128b_x4(t_p + lane_h0, pk[0]);
             ptx::tmem_st_16x128b_x4(t_p + lane_h1, pk[1]);
             // column sums over the warp's 32 rows: lanes sharing lane&3 hold the
@@ -584,19 +594,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             }
             // lane holds chunk column 8*((lane>>3)&3) + 2*(lane&3) + ((lane>>2)&1)
-            // (slot t % NCOL is rewritten at tile t + NCOL, which cannot start
-            // before every warp has loaded S(t+1), i.e. finished tile t)
+            // (slot t % NCOL is rewritten at tile t + NCOL after waiting for
+            // PV(t+NCOL-1), which needs every warp's P(t+NCOL-1), i.e. every
+            // warp -- and so warps 0..3 -- past tile t+1 and its finish_col(t))
             colbuf[slot * 512 + q4 * 128 + 32 * cq + 8 * ((lane >> 3) & 3) + 2 * (lane & 3) +
                    ((lane >> 2) & 1)] = c[0];
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                ptx::mbar_arrive(sy.bar(L::B_P_FULL + pb));
+                ptx::mbar_arrive(sy.bar(L::B_P_FULL));
                 ptx::mbar_arrive(sy.bar(L::B_COL + slot));
             }
-            p_par ^= p_used & (1u << pb);
-            p_used |= 1u << pb;
             if (sw < 4 && t > 0 && !finish_col(t - 1, slot == 0 ? L::NCOL - 1 : slot - 1)) {
                 ok = false;
                 break;
