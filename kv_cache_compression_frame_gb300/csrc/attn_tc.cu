@@ -27,9 +27,9 @@
 // lanes it may access) and 32-column chunk (w - 3) / 4 of every S tile;
 // with the 16x256b load shape a thread holds 4 rows x 8 columns, so row
 // statistics combine across 4 lanes (then across the 4 chunk warps once per
-// sweep) and column sums need a 3-level shuffle
-// reduction (then across the 4 lane quarters in shared memory, one tile
-// behind, so no warp waits for the others within a tile).
+// sweep) and column sums need a 3-level shuffle reduction, then a sum over
+// the 4 lane quarters in shared memory, which the PV-issuer warp does while
+// the softmax warps move on (it waits for every warp's P anyway).
 // Shared-memory bandwidth (128 B/clk/SM) is the scarce resource: an MMA with
 // both operands in shared memory at M = N = 128 consumes all of it, leaving
 // nothing for the TMA writes of the next K/V tiles.  So Q lives in TMEM: the
@@ -68,7 +68,7 @@ struct TcLayout {
     static constexpr int TILE = KCH * CHUNK;            // one K or V tile
     static constexpr int KS = 4, VS = 2;                // K and V pipeline stages
     static constexpr int SB1 = 3;                       // sweep-1 S buffers
-    static constexpr int NCOL = 3;                      // column-sum exchange slots
+    static constexpr int NCOL = 2;                      // column-sum exchange slots
     static constexpr int SW = 16;                       // softmax warps
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KS * TILE;
@@ -86,8 +86,7 @@ struct TcLayout {
     static constexpr int B_P_FREE = B_P_FULL + 1;       // P consumed by PV
     static constexpr int B_O_FULL = B_P_FREE + 1;
     static constexpr int B_DRAIN = B_O_FULL + 1;        // [2] each MMA issuer's teardown
-    static constexpr int B_COL = B_DRAIN + 2;           // [NCOL] column-sum exchange
-    static constexpr int B_STAT = B_COL + NCOL;         // row-statistics exchange
+    static constexpr int B_STAT = B_DRAIN + 2;          // row-statistics exchange
     static constexpr int NBAR = B_STAT + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
@@ -194,7 +193,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         ptx::mbar_init(sy.bar(L::B_P_FULL), L::SW);
         ptx::mbar_init(sy.bar(L::B_P_FREE), 1);
-        for (int c = 0; c < L::NCOL; ++c) ptx::mbar_init(sy.bar(L::B_COL + c), L::SW);
         ptx::mbar_init(sy.bar(L::B_O_FULL), 1);
         ptx::mbar_init(sy.bar(L::B_DRAIN), 1);
         ptx::mbar_init(sy.bar(L::B_DRAIN + 1), 1);
@@ -338,6 +336,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const uint32_t v_hi = (uint32_t)(ptx::sdesc_sw128(0, L::CHUNK, 1024) >> 32);
         const uint32_t vb0 = (uint32_t)ptx::sdesc_sw128(sV, L::CHUNK, 1024);
         uint32_t pv_par = 0;                           // parity of the next P_FULL phase
+        const float* colbuf = reinterpret_cast<const float*>(base + L::OFF_COL);
+        float* colsum = a.colsum + ((int64_t)u * n_rt + mt) * a.m_pad;
         bool ok = true;
         // O overlays sweep-1 S buffer 2: P(0) is written only after every
         // softmax warp finished sweep 1, so PV(0) waiting for P(0) is enough
@@ -366,7 +366,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 else ptx::umma_commit(sy.bar(L::B_V_EMPTY + vs));
             }
             __syncwarp();
-            if (mine) pv_par ^= 1u;
+            if (mine) {
+                pv_par ^= 1u;
+                // key column sums of P(t): the 4 lane quarters' partials
+                const float* cb = colbuf + (t % L::NCOL) * 512;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = 32 * j + lane;
+                    colsum[t * L::BN + e] = cb[e] + cb[128 + e] + cb[256 + e] + cb[384 + e];
+                }
+            }
         }
         if (ptx::elect_one()) {
             if (ok) ptx::umma_commit(sy.bar(L::B_O_FULL));
@@ -524,15 +533,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
         // ---- sweep 2: P, its column sums, P -> TMEM (bf16) for PV
         uint32_t p_par = 0;                            // parity of the P_FREE phase of PV(t-1)
-        // column sums of tile t are summed over the 4 lane quarters during
-        // tile t+1 (by warps 0..3), from slot t % NCOL of the exchange buffer
-        auto finish_col = [&](int t, int slot) -> bool {
-            if (!sy.wait(L::B_COL + slot, (uint32_t)((t / L::NCOL) & 1), kSiteCol)) return false;
-            const int e = sw * 32 + lane;
-            const float* cb = colbuf + slot * 512 + e;
-            colsum[t * L::BN + e] = cb[0] + cb[128] + cb[256] + cb[384];
-            return true;
-        };
         for (int t = 0, slot = 0; ok && t < me.nt; ++t, slot = (slot == L::NCOL - 1) ? 0 : slot + 1) {
             const int b = t & 1;
             if (!sy.wait(L::B_S_FULL + b, (s_par >> b) & 1u, kSiteSFull)) { ok = false; break; }
@@ -593,25 +593,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     c[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
                 }
             }
-            // lane holds chunk column 8*((lane>>3)&3) + 2*(lane&3) + ((lane>>2)&1)
-            // (slot t % NCOL is rewritten at tile t + NCOL after waiting for
-            // PV(t+NCOL-1), which needs every warp's P(t+NCOL-1), i.e. every
-            // warp -- and so warps 0..3 -- past tile t+1 and its finish_col(t))
+            // lane holds chunk column 8*((lane>>3)&3) + 2*(lane&3) + ((lane>>2)&1);
+            // the PV issuer sums the 4 lane quarters once P_FULL(t) (a release
+            // after this store) completes; slot t % NCOL is rewritten at tile
+            // t + NCOL only after PV(t+NCOL-1), which that warp issues after
+            // reading the slot
             colbuf[slot * 512 + q4 * 128 + 32 * cq + 8 * ((lane >> 3) & 3) + 2 * (lane & 3) +
                    ((lane >> 2) & 1)] = c[0];
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(sy.bar(L::B_P_FULL));
-                ptx::mbar_arrive(sy.bar(L::B_COL + slot));
-            }
-            if (sw < 4 && t > 0 && !finish_col(t - 1, slot == 0 ? L::NCOL - 1 : slot - 1)) {
-                ok = false;
-                break;
-            }
+            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_P_FULL));
         }
-        if (ok && sw < 4 && me.nt > 0) ok = finish_col(me.nt - 1, (me.nt - 1) % L::NCOL);
         if (me.nt > 0)
             for (int kk = me.nt * L::BN + sw * 32 + lane; kk < a.m_pad; kk += 32 * L::SW)
                 colsum[kk] = 0.f;
