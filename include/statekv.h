@@ -169,6 +169,28 @@ int statekv_prefill_frame_host(statekv_handle* h, const void* q_host,
                                void* o_host, void* cuda_stream);
 
 /*
+ * `frames` consecutive steps from HOST buffers holding the frames back to
+ * back (frame-major, each frame in the layouts above):
+ *   q, o : [frames][S][L][Hq][T][d]      k, v : [frames][S][L][Hkv][T][d]
+ * The same computation as `frames` calls of statekv_prefill_frame_host, but
+ * the copies overlap the device work: the handle holds two staging slots,
+ * and on two side streams of its own it copies frame i+1 in and frame i-1
+ * out while frame i runs on cuda_stream.  The whole batch is ordered on
+ * cuda_stream like a single call: the side streams first wait for the work
+ * already enqueued there, and cuda_stream waits for the last copy out, so
+ * every o frame is valid (and q/k/v may be reused) once the stream passes
+ * the call.  Host buffers should be page-locked.  Returns E_CAPACITY, with
+ * nothing done, when n + frames > max_frames; frames == 0 is a no-op.  The
+ * side streams and events are created on the first call (E_CUDA if that
+ * fails); a handle's calls must not overlap with each other.
+ * This entry point has no counterpart in the page; it streams a video from
+ * host memory at device speed.
+ */
+int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q_host,
+                                const void* k_host, const void* v_host, void* o_host,
+                                void* cuda_stream);
+
+/*
  * Borrowed DEVICE pointers to the compressed state C_{n-1} of (stream s,
  * layer) after the last step: k, v -> [Hkv][pitch][d], pos -> [Hkv][pitch]
  * int32 virtual positions; the first *count slots of each head are live

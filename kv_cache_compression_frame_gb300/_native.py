@@ -33,7 +33,7 @@ KERNEL_NAMES = ("rope_table", "rope", "attention", "select")
 
 EXPORTS = (
     "statekv_status_string", "statekv_create", "statekv_destroy",
-    "statekv_prefill_frame", "statekv_prefill_frame_host",
+    "statekv_prefill_frame", "statekv_prefill_frame_host", "statekv_prefill_frames_host",
     "statekv_get_compressed", "statekv_get_detailed", "statekv_frame_index",
     "statekv_reset", "statekv_check_device_status", "statekv_get_scores",
     "statekv_get_rotated_query", "statekv_set_frame_index",
@@ -81,6 +81,7 @@ def load() -> C.CDLL:
         "statekv_destroy": (C.c_int, [h]),
         "statekv_prefill_frame": (C.c_int, [h, _P, _P, _P, _P, _P]),
         "statekv_prefill_frame_host": (C.c_int, [h, _P, _P, _P, _P, _P]),
+        "statekv_prefill_frames_host": (C.c_int, [h, C.c_int32, _P, _P, _P, _P, _P]),
         "statekv_get_compressed": (C.c_int, [h, C.c_int32, C.c_int32, _PP, _PP, _PP,
                                              C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
         "statekv_get_detailed": (C.c_int, [h, C.c_int32, C.c_int32, _PP, _PP,

@@ -63,6 +63,12 @@ struct statekv_handle {
     int32_t* score_pos = nullptr;
     uint32_t* err = nullptr;            // device status word
     void* stage_q = nullptr; void* stage_k = nullptr; void* stage_v = nullptr; void* stage_o = nullptr;
+    // second staging slot and the side streams / events of the batched host
+    // entry point (streams and events are created on its first call)
+    void* stage2_q = nullptr; void* stage2_k = nullptr; void* stage2_v = nullptr;
+    void* stage2_o = nullptr;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_entry = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
     TcMaps tc{};                        // TMA views for the bf16 attention kernel
 
     bool profiling = false;
@@ -92,6 +98,11 @@ void free_all(statekv_handle* h) {
     for (auto e : h->spare) cudaEventDestroy(e);
     h->pending.clear();
     h->spare.clear();
+    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0], &h->ev_comp[1],
+                           &h->ev_out[0], &h->ev_out[1]})
+        if (*e) { cudaEventDestroy(*e); *e = nullptr; }
+    for (cudaStream_t* st : {&h->s_in, &h->s_out})
+        if (*st) { cudaStreamDestroy(*st); *st = nullptr; }
 }
 
 template <typename T>
@@ -291,6 +302,10 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     ok = ok && dalloc(h, &h->stage_k, h->kv_bytes());
     ok = ok && dalloc(h, &h->stage_v, h->kv_bytes());
     ok = ok && dalloc(h, &h->stage_o, h->q_bytes());
+    ok = ok && dalloc(h, &h->stage2_q, h->q_bytes());
+    ok = ok && dalloc(h, &h->stage2_k, h->kv_bytes());
+    ok = ok && dalloc(h, &h->stage2_v, h->kv_bytes());
+    ok = ok && dalloc(h, &h->stage2_o, h->q_bytes());
     if (!ok) { free_all(h); delete h; return STATEKV_E_OOM; }
     if (cudaMemcpy(h->omega, om.data(), sizeof(double) * om.size(), cudaMemcpyHostToDevice) !=
         cudaSuccess) {
@@ -341,6 +356,79 @@ int statekv_prefill_frame_host(statekv_handle* h, const void* q, const void* k, 
     if (r != STATEKV_OK) return r;
     if (cudaMemcpyAsync(o, h->stage_o, h->q_bytes(), cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return STATEKV_E_CUDA;
+    return STATEKV_OK;
+}
+
+namespace {
+
+bool ensure_pipeline(statekv_handle* h) {
+    if (h->s_in) return true;
+    bool ok = cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0],
+                           &h->ev_comp[1], &h->ev_out[0], &h->ev_out[1]})
+        ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0],
+                               &h->ev_comp[1], &h->ev_out[0], &h->ev_out[1]})
+            if (*e) { cudaEventDestroy(*e); *e = nullptr; }
+        for (cudaStream_t* st : {&h->s_in, &h->s_out})
+            if (*st) { cudaStreamDestroy(*st); *st = nullptr; }
+        cudaGetLastError();
+    }
+    return ok;
+}
+
+}  // namespace
+
+// Frames i = 0..F-1, staging slot i & 1:
+//   s_in : [wait compute(i-2)] H2D q,k,v(i) -> slot          record ev_in[slot]
+//   st   : wait ev_in[slot], [wait D2H(i-2)] step(i)          record ev_comp[slot]
+//   s_out: wait ev_comp[slot]  D2H o(i) <- slot                record ev_out[slot]
+// so the copies of frames i+1 (in) and i-1 (out) overlap the step of frame i.
+// Both side streams first wait for everything already on st; at the end st
+// waits for the last D2H, so the batch is ordered on st like one call.
+int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q, const void* k,
+                                const void* v, void* o, void* cuda_stream) {
+    if (!h || frames < 0 || !q || !k || !v || !o) return STATEKV_E_INVALID_ARG;
+    if (frames == 0) return STATEKV_OK;
+    if (h->n + frames > h->cfg.max_frames) return STATEKV_E_CAPACITY;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return STATEKV_E_CUDA;
+    if (!ensure_pipeline(h)) return STATEKV_E_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    const size_t qb = h->q_bytes(), kvb = h->kv_bytes();
+    void* sq[2] = {h->stage_q, h->stage2_q};
+    void* sk[2] = {h->stage_k, h->stage2_k};
+    void* sv[2] = {h->stage_v, h->stage2_v};
+    void* so[2] = {h->stage_o, h->stage2_o};
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    if (!ok(cudaEventRecord(h->ev_entry, st)) || !ok(cudaStreamWaitEvent(h->s_in, h->ev_entry, 0)) ||
+        !ok(cudaStreamWaitEvent(h->s_out, h->ev_entry, 0)))
+        return STATEKV_E_CUDA;
+    for (int32_t i = 0; i < frames; ++i) {
+        const int sl = i & 1;
+        const char* qi = static_cast<const char*>(q) + (size_t)i * qb;
+        const char* ki = static_cast<const char*>(k) + (size_t)i * kvb;
+        const char* vi = static_cast<const char*>(v) + (size_t)i * kvb;
+        char* oi = static_cast<char*>(o) + (size_t)i * qb;
+        if (i >= 2 && !ok(cudaStreamWaitEvent(h->s_in, h->ev_comp[sl], 0))) return STATEKV_E_CUDA;
+        if (!ok(cudaMemcpyAsync(sq[sl], qi, qb, cudaMemcpyHostToDevice, h->s_in)) ||
+            !ok(cudaMemcpyAsync(sk[sl], ki, kvb, cudaMemcpyHostToDevice, h->s_in)) ||
+            !ok(cudaMemcpyAsync(sv[sl], vi, kvb, cudaMemcpyHostToDevice, h->s_in)) ||
+            !ok(cudaEventRecord(h->ev_in[sl], h->s_in)) ||
+            !ok(cudaStreamWaitEvent(st, h->ev_in[sl], 0)))
+            return STATEKV_E_CUDA;
+        if (i >= 2 && !ok(cudaStreamWaitEvent(st, h->ev_out[sl], 0))) return STATEKV_E_CUDA;
+        const int r = run_frame(h, sq[sl], sk[sl], sv[sl], so[sl], st);
+        if (r != STATEKV_OK) return r;
+        if (!ok(cudaEventRecord(h->ev_comp[sl], st)) ||
+            !ok(cudaStreamWaitEvent(h->s_out, h->ev_comp[sl], 0)) ||
+            !ok(cudaMemcpyAsync(oi, so[sl], qb, cudaMemcpyDeviceToHost, h->s_out)) ||
+            !ok(cudaEventRecord(h->ev_out[sl], h->s_out)))
+            return STATEKV_E_CUDA;
+    }
+    if (!ok(cudaStreamWaitEvent(st, h->ev_out[(frames - 1) & 1], 0))) return STATEKV_E_CUDA;
     return STATEKV_OK;
 }
 

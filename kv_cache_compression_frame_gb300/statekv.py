@@ -150,6 +150,21 @@ class StateKV:
             _stream_ptr(stream, self.device)), "statekv_prefill_frame_host")
         return o
 
+    def prefill_frames_host(self, q, k, v, o, stream=None) -> torch.Tensor:
+        """F consecutive frame steps from frame-major host tensors
+        q, o [F][S][L][Hq][T][d], k, v [F][S][L][Hkv][T][d] (pinned), with
+        the copies overlapping the device work; ordered on `stream` as one call."""
+        frames = q.shape[0] if q.dim() == len(self.q_shape) + 1 else -1
+        if frames < 0:
+            raise ValueError(f"q: want [F] + {self.q_shape}, got {tuple(q.shape)}")
+        for t, s, nme in ((q, self.q_shape, "q"), (k, self.kv_shape, "k"),
+                          (v, self.kv_shape, "v"), (o, self.q_shape, "o")):
+            self._check_in(t, (frames,) + tuple(s), nme, device=False)
+        N.check(self._lib.statekv_prefill_frames_host(
+            self._h, frames, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            _stream_ptr(stream, self.device)), "statekv_prefill_frames_host")
+        return o
+
     # ------------------------------------------------------------- state
     @property
     def frame_index(self) -> int:

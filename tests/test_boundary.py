@@ -74,6 +74,7 @@ def test_null_handle_and_pointers(lib):
     assert lib.statekv_destroy(None) == N.OK
     assert lib.statekv_prefill_frame(None, None, None, None, None, None) == N.E_INVALID_ARG
     assert lib.statekv_prefill_frame_host(None, None, None, None, None, None) == N.E_INVALID_ARG
+    assert lib.statekv_prefill_frames_host(None, 1, None, None, None, None, None) == N.E_INVALID_ARG
     assert lib.statekv_reset(None) == N.E_INVALID_ARG
     assert lib.statekv_frame_index(None) == -1
     assert lib.statekv_set_frame_index(None, 0) == N.E_INVALID_ARG

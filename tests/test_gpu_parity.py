@@ -250,6 +250,40 @@ def test_host_entry_point_matches_device_entry_point():
         assert raw_equal(ka[:, :ca], kb[:, :cb])
 
 
+@pytest.mark.parametrize("chunks", [(5,), (1, 2, 3)])
+def test_batched_host_entry_point_matches_device_entry_point(chunks):
+    """Frames streamed from host memory with overlapped copies give the same
+    bits as one device call per frame, whatever the batch boundaries."""
+    sh = _small("hostbatch", q_heads=4, kv_heads=2, head_dim=128, frame_tokens=64,
+                budget=128, frames=6)
+    a, b = Stepper(sh), Stepper(sh)
+    F = sum(chunks)
+    tens = [a.tensors(n)[1] for n in range(F)]
+    o_dev = [a.h.prefill_frame(q, k, v).cpu() for q, k, v in tens]
+    hq = torch.stack([t[0].cpu() for t in tens]).pin_memory()
+    hk = torch.stack([t[1].cpu() for t in tens]).pin_memory()
+    hv = torch.stack([t[2].cpu() for t in tens]).pin_memory()
+    ho = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
+    f0 = 0
+    for c in chunks:
+        b.h.prefill_frames_host(hq[f0:f0 + c], hk[f0:f0 + c], hv[f0:f0 + c], ho[f0:f0 + c])
+        f0 += c
+    torch.cuda.synchronize()
+    b.h.check_device_status()
+    assert b.h.frame_index == F
+    for n in range(F):
+        assert raw_equal(o_dev[n], ho[n]), f"O frame {n}"
+    ka, va, pa, ca = a.h.compressed(0, 0)
+    kb, vb, pb, cb = b.h.compressed(0, 0)
+    assert ca == cb and torch.equal(pa[:, :ca], pb[:, :cb])
+    assert raw_equal(ka[:, :ca], kb[:, :cb]) and raw_equal(va[:, :ca], vb[:, :cb])
+    # a batch past max_frames is rejected before any work
+    from kv_cache_compression_frame_gb300 import StateKVError
+    with pytest.raises(StateKVError) as ei:
+        b.h.prefill_frames_host(hq[:2], hk[:2], hv[:2], ho[:2])
+    assert ei.value.status == -3 and b.h.frame_index == F
+
+
 def test_reset_replays_bit_identically():
     sh = _small("replay", q_heads=4, kv_heads=2, head_dim=64, frame_tokens=64,
                 budget=96, frames=4)
