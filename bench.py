@@ -210,7 +210,8 @@ def run_gpu(args, sh):
     dk = [torch.from_numpy(r[1]).to(torch.bfloat16).to(dev) for r in ring]
     dv = [torch.from_numpy(r[2]).to(torch.bfloat16).to(dev) for r in ring]
     o = torch.empty_like(dq[0])
-    h = StateKV(StateKVConfig.from_shape(sh, max_frames=frames), device=local)
+    # one frame of extra detailed-state rows: room for the text of the decode leg
+    h = StateKV(StateKVConfig.from_shape(sh, max_frames=frames + 1), device=local)
     stream = torch.cuda.current_stream(dev)
 
     def one_video():
@@ -310,6 +311,45 @@ def run_gpu(args, sh):
                "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b,
                "steps": args.e2e_steps}
 
+    # decode leg: after a whole video, single text tokens over the detailed
+    # state D (every frame's K/V); HBM-bound, algorithmic bytes = K and V of
+    # every D row read once per step
+    dec = None
+    if not args.no_decode and sh.head_dim == 128:
+        h.reset()
+        for n in range(frames):
+            r = n % RING
+            h.prefill_frame(dq[r], dk[r], dv[r], o, stream)
+        g = torch.Generator(device="cpu").manual_seed(5)
+        tq = torch.randn((sh.streams, sh.layers, sh.q_heads, 1, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
+        tk = torch.randn((sh.streams, sh.layers, sh.kv_heads, 1, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
+        tv = torch.randn((sh.streams, sh.layers, sh.kv_heads, 1, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
+        to = torch.empty_like(tq)
+        for _ in range(3):
+            h.decode(tq, tk, tv, to, stream)
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        k0 = frames * sh.frame_tokens + h.text_tokens
+        n_dec = args.decode_steps
+        torch.cuda.synchronize()
+        d0.record(stream)
+        for _ in range(n_dec):
+            h.decode(tq, tk, tv, to, stream)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        h.check_device_status()
+        dms = d0.elapsed_time(d1) / n_dec
+        units = sh.streams * sh.layers * sh.kv_heads
+        rows = k0 + (n_dec + 1) / 2.0                       # mean D rows read per step
+        dbytes = units * rows * sh.head_dim * 2 * 2
+        dec = {"tokens_per_s": 1000.0 / dms, "us_per_step": dms * 1000.0,
+               "d_rows_per_kv_head": int(k0), "steps": n_dec,
+               "roofline": {"bound": "hbm", "achieved": dbytes / (dms / 1000.0) / 1e9,
+                            "peak": peaks["hbm"], "unit": "GB/s",
+                            "frac": dbytes / (dms / 1000.0) / 1e9 / peaks["hbm"],
+                            "bytes_per_step": dbytes,
+                            "kernel": "decode_kernel + decode_combine_kernel"}}
+
     # roofline of the dominant kernel (attention) over the timed region
     flops_timed = args.steps * sum(sh.attention_flops(n) for n in range(frames))
     attn_ms, attn_n = prof["attention"]
@@ -354,6 +394,7 @@ def run_gpu(args, sh):
                              "steady_p99": sorted(steady)[int(0.99 * (len(steady) - 1))] if steady else None,
                              "last_quarter_over_first_quarter": flat},
             "e2e": e2e,
+            "decode": dec,
             "gpu_launches": sum(c for _, c in prof.values()),
             "clocks": clk,
         }
@@ -374,6 +415,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--frames", type=int, default=0, help="frames per video (default: N of the workload)")
     ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--decode-steps", type=int, default=20)
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -191,6 +191,30 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
                                 void* cuda_stream);
 
 /*
+ * Text decode over the detailed state (关键设计 1: D_n keeps every frame's
+ * K/V for text decoding; 关键设计 3: text continues the virtual positions
+ * with the same static scale).  `tokens` new text tokens (1..16, and at most
+ * T) take positions p = position_offset + n*T + j, j counting every text
+ * token decoded since the last frame; their K', V are appended to D after
+ * the rows already there, and each query row attends over all earlier D rows
+ * (the whole video and earlier text) and, causally, over the new tokens:
+ *   O = softmax(Q' [D_K]^T * mscale^2/sqrt(d), causal on the new rows) D_V.
+ * Device pointers, contiguous, storage dtype:
+ *   q, o : [S][L][Hq][tokens][d]     k, v : [S][L][Hkv][tokens][d] (pre-RoPE)
+ * Supported: bf16 storage, d = 128, G*tokens <= 64 (else E_UNSUPPORTED).
+ * Returns E_CAPACITY (nothing done) when the new rows do not fit in D
+ * (n*T + decoded + tokens > max_frames*T).  Once a handle has decoded text,
+ * the prefill entry points return E_INVALID_ARG until statekv_reset.  The
+ * first call allocates the handle's decode scratch (partial results per
+ * 2048-key chunk of D; E_OOM if that fails).
+ */
+int statekv_decode(statekv_handle* h, int32_t tokens, const void* q, const void* k,
+                   const void* v, void* o, void* cuda_stream);
+
+/* Text tokens decoded since the last reset (-1 for a NULL handle). */
+int64_t statekv_text_tokens(const statekv_handle* h);
+
+/*
  * Borrowed DEVICE pointers to the compressed state C_{n-1} of (stream s,
  * layer) after the last step: k, v -> [Hkv][pitch][d], pos -> [Hkv][pitch]
  * int32 virtual positions; the first *count slots of each head are live
@@ -204,7 +228,7 @@ int statekv_get_compressed(statekv_handle* h, int32_t s, int32_t layer,
 /*
  * Borrowed DEVICE pointers to the detailed state D_{n-1} of (s, layer):
  * k, v -> [Hkv][pitch][d] with row r = virtual position r - position_offset
- * (post-RoPE K, V as given); *count = n*T live rows per head,
+ * (post-RoPE K, V as given); *count = n*T (+ decoded text tokens) live rows per head,
  * *pitch = max_frames*T.  Any output pointer may be NULL.
  */
 int statekv_get_detailed(statekv_handle* h, int32_t s, int32_t layer,

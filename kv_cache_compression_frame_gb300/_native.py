@@ -38,7 +38,7 @@ EXPORTS = (
     "statekv_reset", "statekv_check_device_status", "statekv_get_scores",
     "statekv_get_rotated_query", "statekv_set_frame_index",
     "statekv_set_compressed", "statekv_profile_enable", "statekv_profile_read",
-    "statekv_attend_scores_static",
+    "statekv_attend_scores_static", "statekv_decode", "statekv_text_tokens",
 )
 
 
@@ -87,6 +87,8 @@ def load() -> C.CDLL:
         "statekv_get_detailed": (C.c_int, [h, C.c_int32, C.c_int32, _PP, _PP,
                                            C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
         "statekv_frame_index": (C.c_int64, [h]),
+        "statekv_decode": (C.c_int, [h, C.c_int32, _P, _P, _P, _P, _P]),
+        "statekv_text_tokens": (C.c_int64, [h]),
         "statekv_reset": (C.c_int, [h]),
         "statekv_check_device_status": (C.c_int, [h, _P]),
         "statekv_get_scores": (C.c_int, [h, C.c_int32, C.c_int32, _PP, _PP,

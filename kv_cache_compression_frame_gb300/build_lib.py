@@ -24,7 +24,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libstatekv.so")
 
 SOURCES = ["statekv_api.cu", "rope.cu", "attn_tc.cu", "attn_simt.cu", "select.cu",
-           "attend_static.cu"]
+           "attend_static.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                  "-I", INCLUDE, "-I", CSRC]

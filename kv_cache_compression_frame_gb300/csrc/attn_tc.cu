@@ -52,13 +52,10 @@
 
 #include <cstdlib>
 
-#include "statekv_internal.cuh"
-#include "sm100_ptx.cuh"
+#include "pipeline.cuh"
 
 namespace statekv {
 namespace {
-
-constexpr uint64_t kTimeoutNs = 1000000000ull;   // 1 s per wait
 
 template <int D>
 struct TcLayout {
@@ -93,44 +90,6 @@ struct TcLayout {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_O = 256, TM_P = 384, TM_Q = 448;
     static constexpr int THREADS = 96 + 32 * SW;
-};
-
-struct Sync {
-    uint32_t bar0;                 // smem address of barrier 0
-    volatile uint32_t* abort;      // CTA-wide abort flag (smem)
-    uint32_t* err;
-
-    __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
-
-    // Wait for the phase of the given parity; gives up on abort or timeout.
-    // After one non-blocking probe the thread sleeps in try_wait, which
-    // returns as soon as the phase completes (a spin that also reads the
-    // global timer reacts hundreds of cycles late).
-    __device__ bool wait(int i, uint32_t parity, uint32_t site) const {
-        const uint32_t b = bar(i);
-        if (ptx::mbar_poll(b, parity)) return true;
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-            if (ptx::mbar_wait_hint(b, parity, 20000u)) return true;
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kTimeoutNs) {
-                *abort = 1u;
-                record_error(err, (uint32_t)STATEKV_E_TIMEOUT, site, (uint32_t)i);
-                return false;
-            }
-        }
-    }
-    // Teardown wait: ignores the abort flag, still bounded.
-    __device__ void drain(int i, uint32_t parity) const {
-        const uint32_t b = bar(i);
-        const uint64_t t0 = globaltimer_ns();
-        while (!ptx::mbar_wait_hint(b, parity, 20000u)) {
-            if (globaltimer_ns() - t0 > kTimeoutNs) {
-                record_error(err, (uint32_t)STATEKV_E_TIMEOUT, kSiteDrain, (uint32_t)i);
-                return;
-            }
-        }
-    }
 };
 
 // Key range of one 128-row query tile: tiles [0, nt) hold a key visible to
@@ -664,7 +623,9 @@ cudaError_t launch_tc(const AttnArgs& a, const TcMaps& m, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, CS>, m.k, m.v, a);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* p = nullptr;
@@ -677,8 +638,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D bf16 view [units][rows][d] read in boxes of 64 columns (one 128-byte
-// swizzle row) x box_rows rows.
 bool encode_view(CUtensorMap* m, const void* base, int d, int64_t rows, int64_t units,
                  int box_rows) {
     auto enc = tensor_map_encoder();
@@ -692,8 +651,6 @@ bool encode_view(CUtensorMap* m, const void* base, int d, int64_t rows, int64_t 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
-
-}  // namespace
 
 int tc_cluster_size(int n_row_tiles) {
     // CTAs of a cluster are consecutive query tiles of one unit.  Sharing

@@ -13,7 +13,7 @@
 //    fp64 (T*d/2 angles per frame, shared by every head and layer);
 //  * rope: one pass over Q, K and V of all (stream, layer, head) rows.
 //    Q' goes to scratch; K' and V go to the compressed pool after its c live
-//    slots and to D rows [nT, nT+T).  16-byte vector loads/stores, rows of
+//    slots and to D rows [nT, nT+T) (text tokens being decoded: D only).  16-byte vector loads/stores, rows of
 //    d/2 + d/2 pairs handled by d/(2*VEC) threads each.
 #include "statekv_internal.cuh"
 
@@ -110,10 +110,12 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
         return;
     }
     const int64_t unit = src_row / a.T;
-    E* pool = (E*)(kind == 1 ? a.pool_k : a.pool_v) + (unit * a.slots + a.c + i) * a.d;
+    if (a.pool_k) {                                  // text tokens go to D only
+        E* pool = (E*)(kind == 1 ? a.pool_k : a.pool_v) + (unit * a.slots + a.c + i) * a.d;
+        *reinterpret_cast<uint4*>(pool + k0) = lo;
+        *reinterpret_cast<uint4*>(pool + half + k0) = hi;
+    }
     E* det = (E*)(kind == 1 ? a.det_k : a.det_v) + (unit * a.det_pitch + a.det_row0 + i) * a.d;
-    *reinterpret_cast<uint4*>(pool + k0) = lo;
-    *reinterpret_cast<uint4*>(pool + half + k0) = hi;
     *reinterpret_cast<uint4*>(det + k0) = lo;
     *reinterpret_cast<uint4*>(det + half + k0) = hi;
 }

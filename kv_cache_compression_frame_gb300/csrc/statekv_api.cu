@@ -47,6 +47,10 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 struct statekv_handle {
     statekv_config cfg{};
     int64_t n = 0;                      // frames processed
+    int64_t text = 0;                   // text tokens decoded after frame n-1
+    int num_sms = 0;
+    float* dec_m = nullptr; float* dec_l = nullptr; float* dec_o = nullptr;  // decode partials
+    int64_t dec_items = 0;              // capacity of the partials (items)
     int G = 0, U = 0, GT = 0, slots = 0, m_pad = 0, n_row_tiles = 0, esize = 0;
     int64_t det_pitch = 0;
     double mscale = 1.0;
@@ -315,6 +319,10 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
         !make_tc_maps(&h->tc, h->pool_k, h->pool_v, d, h->slots, h->U, h->n_row_tiles)) {
         free_all(h); delete h; return STATEKV_E_CUDA;
     }
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c.device) !=
+        cudaSuccess) {
+        free_all(h); delete h; return STATEKV_E_CUDA;
+    }
     if (cudaDeviceSynchronize() != cudaSuccess) { free_all(h); delete h; return STATEKV_E_CUDA; }
     *out = h;
     return STATEKV_OK;
@@ -335,6 +343,7 @@ int statekv_prefill_frame(statekv_handle* h, const void* q, const void* k, const
     int r;
     if ((r = check_ptr(q)) || (r = check_ptr(k)) || (r = check_ptr(v)) || (r = check_ptr(o)))
         return r;
+    if (h->text > 0) return STATEKV_E_INVALID_ARG;   // decoding has started: reset first
     if (h->n >= h->cfg.max_frames) return STATEKV_E_CAPACITY;
     DeviceGuard g(h->cfg.device);
     if (!g.ok) return STATEKV_E_CUDA;
@@ -343,7 +352,7 @@ int statekv_prefill_frame(statekv_handle* h, const void* q, const void* k, const
 
 int statekv_prefill_frame_host(statekv_handle* h, const void* q, const void* k, const void* v,
                                void* o, void* cuda_stream) {
-    if (!h || !q || !k || !v || !o) return STATEKV_E_INVALID_ARG;
+    if (!h || !q || !k || !v || !o || h->text > 0) return STATEKV_E_INVALID_ARG;
     if (h->n >= h->cfg.max_frames) return STATEKV_E_CAPACITY;
     DeviceGuard g(h->cfg.device);
     if (!g.ok) return STATEKV_E_CUDA;
@@ -390,7 +399,7 @@ bool ensure_pipeline(statekv_handle* h) {
 // waits for the last D2H, so the batch is ordered on st like one call.
 int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q, const void* k,
                                 const void* v, void* o, void* cuda_stream) {
-    if (!h || frames < 0 || !q || !k || !v || !o) return STATEKV_E_INVALID_ARG;
+    if (!h || frames < 0 || !q || !k || !v || !o || h->text > 0) return STATEKV_E_INVALID_ARG;
     if (frames == 0) return STATEKV_OK;
     if (h->n + frames > h->cfg.max_frames) return STATEKV_E_CAPACITY;
     DeviceGuard g(h->cfg.device);
@@ -432,6 +441,59 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
     return STATEKV_OK;
 }
 
+int statekv_decode(statekv_handle* h, int32_t tokens, const void* q, const void* k, const void* v,
+                   void* o, void* cuda_stream) {
+    if (!h) return STATEKV_E_INVALID_ARG;
+    int r;
+    if ((r = check_ptr(q)) || (r = check_ptr(k)) || (r = check_ptr(v)) || (r = check_ptr(o)))
+        return r;
+    const statekv_config& c = h->cfg;
+    if (tokens < 1 || tokens > 16 || tokens > c.frame_tokens) return STATEKV_E_INVALID_ARG;
+    if (c.dtype != STATEKV_BF16 || c.head_dim != 128) return STATEKV_E_UNSUPPORTED;
+    const int R = h->G * tokens;
+    const int npad = decode_rows_pad(R);
+    if (npad < 0) return STATEKV_E_UNSUPPORTED;
+    const int64_t visible = h->n * c.frame_tokens + h->text;
+    if (visible + tokens > h->det_pitch) return STATEKV_E_CAPACITY;
+    DeviceGuard g(c.device);
+    if (!g.ok) return STATEKV_E_CUDA;
+    // partial-result buffers, sized once for the whole detailed state
+    const int64_t items_max = (int64_t)h->U * decode_chunks(h->det_pitch);
+    if (h->dec_items < items_max) {
+        if (!dalloc(h, &h->dec_m, sizeof(float) * items_max * 64) ||
+            !dalloc(h, &h->dec_l, sizeof(float) * items_max * 64) ||
+            !dalloc(h, &h->dec_o, sizeof(float) * items_max * 64 * 128))
+            return STATEKV_E_OOM;
+        h->dec_items = items_max;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    const int64_t p0 = c.position_offset + visible;
+    RopeTableArgs ta{h->omega, h->cs, p0, tokens, c.head_dim / 2};
+    if (launch_rope_table(ta, st) != cudaSuccess) return STATEKV_E_CUDA;
+    RopeArgs ra{};
+    ra.q = q; ra.k = k; ra.v = v;
+    ra.q_rot = h->q_rot; ra.pool_k = nullptr; ra.pool_v = nullptr;
+    ra.det_k = h->det_k; ra.det_v = h->det_v; ra.cs = h->cs;
+    ra.rows_q = (int64_t)h->U * R;
+    ra.rows_kv = (int64_t)h->U * tokens;
+    ra.T = tokens; ra.d = c.head_dim; ra.slots = h->slots; ra.c = 0;
+    ra.det_pitch = h->det_pitch; ra.det_row0 = visible;
+    if (launch_rope(ra, c.dtype, st) != cudaSuccess) return STATEKV_E_CUDA;
+    DecodeMaps maps;
+    if (!make_decode_maps(&maps, h->q_rot, R, npad, h->det_k, h->det_v, h->det_pitch, h->U))
+        return STATEKV_E_CUDA;
+    DecodeArgs da{};
+    da.o = o; da.part_m = h->dec_m; da.part_l = h->dec_l; da.part_o = h->dec_o; da.err = h->err;
+    da.U = h->U; da.R = R; da.tok = tokens; da.chunks = decode_chunks(visible + tokens);
+    da.num_sms = h->num_sms; da.visible = visible; da.keys = visible + tokens;
+    da.scale_log2 = h->scale_log2;
+    if (launch_decode(da, maps, st) != cudaSuccess) return STATEKV_E_CUDA;
+    h->text += tokens;
+    return STATEKV_OK;
+}
+
+int64_t statekv_text_tokens(const statekv_handle* h) { return h ? h->text : -1; }
+
 int statekv_get_compressed(statekv_handle* h, int32_t s, int32_t layer, const void** k,
                            const void** v, const int32_t** pos, int32_t* count, int32_t* pitch) {
     if (!h || s < 0 || s >= h->cfg.num_streams || layer < 0 || layer >= h->cfg.num_layers)
@@ -454,7 +516,7 @@ int statekv_get_detailed(statekv_handle* h, int32_t s, int32_t layer, const void
     const size_t row = (size_t)h->cfg.head_dim * h->esize;
     if (k) *k = (const char*)h->det_k + u0 * h->det_pitch * row;
     if (v) *v = (const char*)h->det_v + u0 * h->det_pitch * row;
-    if (count) *count = h->n * h->cfg.frame_tokens;
+    if (count) *count = h->n * h->cfg.frame_tokens + h->text;
     if (pitch) *pitch = h->det_pitch;
     return STATEKV_OK;
 }
@@ -464,6 +526,7 @@ int64_t statekv_frame_index(const statekv_handle* h) { return h ? h->n : -1; }
 int statekv_reset(statekv_handle* h) {
     if (!h) return STATEKV_E_INVALID_ARG;
     h->n = 0;
+    h->text = 0;
     return STATEKV_OK;
 }
 

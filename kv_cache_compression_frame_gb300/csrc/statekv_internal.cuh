@@ -79,6 +79,27 @@ bool make_tc_maps(TcMaps* m, const void* pool_k, const void* pool_v, int d, int6
                   int64_t units, int n_row_tiles);
 cudaError_t launch_attention_tc(const AttnArgs& a, const TcMaps& maps, cudaStream_t st);
 cudaError_t launch_attention_simt(const AttnArgs& a, cudaStream_t st);
+
+// Text decode over the detailed state (decode.cu): R = G*tok query rows per
+// unit, keys = visible + tok D rows, partials per (unit, key chunk).
+struct DecodeArgs {
+    void* o;                     // [U][R][128] bf16
+    float* part_m;               // [U*chunks][npad]  row reference (log2 units)
+    float* part_l;               // [U*chunks][npad]  row sum
+    float* part_o;               // [U*chunks][npad][128] unnormalised O
+    uint32_t* err;
+    int32_t U, R, tok, chunks, num_sms;
+    int64_t visible, keys;
+    float scale_log2;
+};
+struct DecodeMaps {
+    CUtensorMap q, k, v;
+};
+int decode_rows_pad(int R);            // 16 / 32 / 64, or -1 when R > 64
+int decode_chunks(int64_t keys);       // key chunks per unit
+bool make_decode_maps(DecodeMaps* m, const void* q_rot, int R, int npad, const void* det_k,
+                      const void* det_v, int64_t det_pitch, int64_t units);
+cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps& m, cudaStream_t st);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
 // Query-row tile heights of the two attention paths (the column-sum buffer

@@ -165,6 +165,27 @@ class StateKV:
             _stream_ptr(stream, self.device)), "statekv_prefill_frames_host")
         return o
 
+    def decode(self, q, k, v, o=None, stream=None) -> torch.Tensor:
+        """Text tokens over the detailed state: q [S][L][Hq][tok][d],
+        k, v [S][L][Hkv][tok][d] (device, pre-RoPE).  Returns o like q."""
+        tok = q.shape[3] if q.dim() == 5 else -1
+        qs = self.q_shape[:3] + (tok, self.q_shape[4])
+        ks = self.kv_shape[:3] + (tok, self.kv_shape[4])
+        self._check_in(q, qs, "q")
+        self._check_in(k, ks, "k")
+        self._check_in(v, ks, "v")
+        if o is None:
+            o = torch.empty(qs, dtype=self.torch_dtype, device=self.device)
+        self._check_in(o, qs, "o")
+        N.check(self._lib.statekv_decode(
+            self._h, tok, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            _stream_ptr(stream, self.device)), "statekv_decode")
+        return o
+
+    @property
+    def text_tokens(self) -> int:
+        return int(self._lib.statekv_text_tokens(self._h))
+
     # ------------------------------------------------------------- state
     @property
     def frame_index(self) -> int:

@@ -235,6 +235,34 @@ def prefill_unit_frame(state: UnitState, q: np.ndarray, k: np.ndarray,
     return O, info
 
 
+# ------------------------------------------ text decode over D (关键设计 1, 3)
+def decode_unit_tokens(state: UnitState, q: np.ndarray, k: np.ndarray,
+                       v: np.ndarray, first_row: int, *, omega: np.ndarray,
+                       scale: float, dtype: str, position_offset: int = 0):
+    """Text tokens of one (stream, layer, KV head) after the video.
+
+    The detailed state keeps every frame's K/V for text decoding (关键设计 1);
+    text continues the virtual positions with the same static scale
+    (关键设计 3).  q: [G, tok, d], k, v: [tok, d] pre-RoPE; the tokens take
+    D rows first_row.. and positions offset + first_row + j.  Every earlier D
+    row is visible, the new tokens causally (the frame rule of attend_frame
+    with the whole of D in the place of the compressed keys).  Appends K', V
+    to D; returns (O [G, tok, d], q_rot, k_rot).
+    """
+    tok = k.shape[0]
+    pos = position_offset + first_row + np.arange(tok, dtype=np.int64)
+    q_rot = round_to_storage(rope_rotate(q, pos, omega), dtype)
+    k_rot = round_to_storage(rope_rotate(k, pos, omega), dtype)
+    v = np.asarray(v, np.float64)
+    dk, dv = state.detailed_k, state.detailed_v
+    assert dk.shape[0] == first_row
+    O, _ = attend_frame(q_rot, np.concatenate([dk, k_rot]), np.concatenate([dv, v]),
+                        first_row, scale)
+    state.det_k.append(k_rot)
+    state.det_v.append(v)
+    return O, q_rot, k_rot
+
+
 class StateKVOracle:
     """All (stream, layer, KV head) units of one configuration.
 
@@ -250,6 +278,7 @@ class StateKVOracle:
         self.offset = int(getattr(cfg, "position_offset", 0))
         self.group = cfg.q_heads // cfg.kv_heads
         self.n = 0
+        self.text = 0                      # text tokens decoded after the video
         self.units = {(s, l, h): UnitState(cfg.head_dim)
                       for s in range(cfg.streams) for l in range(cfg.layers)
                       for h in range(cfg.kv_heads)}
@@ -271,3 +300,18 @@ class StateKVOracle:
                 infos[(s, l, h)] = info
         self.n += 1
         return (O, infos) if keep_info else O
+
+    def decode(self, q, k, v):
+        """Text tokens after the frames: q [S][L][Hq][tok][d], k, v
+        [S][L][Hkv][tok][d].  Returns O with q's shape (float64)."""
+        cfg, G = self.cfg, self.group
+        O = np.zeros(np.shape(q), np.float64)
+        first = self.n * cfg.frame_tokens + self.text
+        for (s, l, h), st in self.units.items():
+            o, _, _ = decode_unit_tokens(
+                st, q[s][l][h * G:(h + 1) * G], k[s][l][h], v[s][l][h], first,
+                omega=self.omega, scale=self.scale, dtype=cfg.dtype,
+                position_offset=self.offset)
+            O[s, l, h * G:(h + 1) * G] = o
+        self.text += np.shape(k)[3]
+        return O

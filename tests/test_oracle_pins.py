@@ -137,6 +137,40 @@ def check_full_sa_when_budget_covers_all(o=orc):
     np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
 
 
+def check_decode_is_full_causal_over_the_stream(o=orc):
+    """Text decoded after N frames (in two calls) must equal the last rows of
+    ordinary causal self-attention over the whole token sequence (video then
+    text, positions 0..), whatever the budget B: decode reads the detailed
+    state D, which holds every row.  B = 1 evicts almost everything from C."""
+    G, T, d, N = 2, 4, 8, 3
+    theta = 1e4
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((N, G, T, d))
+    k = rng.standard_normal((N, T, d))
+    v = rng.standard_normal((N, T, d))
+    tq = rng.standard_normal((G, 3, d))
+    tk = rng.standard_normal((3, d))
+    tv = rng.standard_normal((3, d))
+    omega, ms = o.rope_frequencies(d, theta)
+    scale = o.logit_scale(d, ms)
+    qs = np.concatenate([q.transpose(0, 2, 1, 3).reshape(N * T, G, d), tq.transpose(1, 0, 2)])
+    want = _brute_full_causal(qs, np.concatenate([k.reshape(N * T, d), tk]),
+                              np.concatenate([v.reshape(N * T, d), tv]), theta,
+                              1.0 / math.sqrt(d), G)[N * T:]       # [3, G, d]
+    for budget in (N * T, 1):
+        state = o.UnitState(d)
+        for n in range(N):
+            o.prefill_unit_frame(state, q[n], k[n], v[n], n, budget=budget,
+                                 omega=omega, scale=scale, dtype="f32")
+        o1, _, _ = o.decode_unit_tokens(state, tq[:, :1], tk[:1], tv[:1], N * T,
+                                        omega=omega, scale=scale, dtype="f32")
+        o2, _, _ = o.decode_unit_tokens(state, tq[:, 1:], tk[1:], tv[1:], N * T + 1,
+                                        omega=omega, scale=scale, dtype="f32")
+        got = np.concatenate([o1, o2], axis=1).transpose(1, 0, 2)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+        assert state.detailed_k.shape[0] == N * T + 3
+
+
 def check_zero_budget_is_per_frame_causal(o=orc):
     """B = 0: no cross-frame state, so each frame is plain causal attention
     over its own tokens -- torch's scaled_dot_product_attention in fp64."""
@@ -194,6 +228,10 @@ def test_rope_is_complex_rotation():
 
 def test_full_sa_special_case():
     check_full_sa_when_budget_covers_all()
+
+
+def test_decode_matches_full_causal_over_the_stream():
+    check_decode_is_full_causal_over_the_stream()
 
 
 def test_zero_budget_matches_sdpa():
@@ -396,14 +434,42 @@ def _mut_pv_transposed_heads(monkeypatch):
 
 
 _CHECKS = [check_golden_zero_keys, check_rope_complex,
-           check_full_sa_when_budget_covers_all,
+           check_full_sa_when_budget_covers_all, check_decode_is_full_causal_over_the_stream,
            check_zero_budget_is_per_frame_causal, check_topb_rank_definition]
+
+
+def _mut_decode_reads_compressed(monkeypatch):
+    def bad(state, q, k, v, first_row, *, omega, scale, dtype, position_offset=0):
+        tok = k.shape[0]
+        pos = position_offset + first_row + np.arange(tok, dtype=np.int64)
+        q_rot = orc.round_to_storage(orc.rope_rotate(q, pos, omega), dtype)
+        k_rot = orc.round_to_storage(orc.rope_rotate(k, pos, omega), dtype)
+        c = state.comp_k.shape[0]
+        O, _ = orc.attend_frame(q_rot, np.concatenate([state.comp_k, k_rot]),
+                                np.concatenate([state.comp_v, v]), c, scale)
+        state.det_k.append(k_rot)
+        state.det_v.append(np.asarray(v, np.float64))
+        return O, q_rot, k_rot
+    monkeypatch.setattr(orc, "decode_unit_tokens", bad)
+
+
+def _mut_decode_position_restart(monkeypatch):
+    good = orc.decode_unit_tokens
+    def bad(state, q, k, v, first_row, **kw):
+        return good(state, q, k, v, first_row, **kw) if first_row == 0 else \
+            _shifted(good, state, q, k, v, first_row, kw)
+    def _shifted(fn, state, q, k, v, first_row, kw):
+        kw = dict(kw)
+        kw["position_offset"] = kw.get("position_offset", 0) - first_row   # text from p = 0
+        return fn(state, q, k, v, first_row, **kw)
+    monkeypatch.setattr(orc, "decode_unit_tokens", bad)
 
 
 @pytest.mark.parametrize("mutation", [
     _mut_mask_offbyone, _mut_score_visible_mean, _mut_tiebreak_high,
     _mut_rope_sign, _mut_rope_freq_index, _mut_no_scale,
-    _mut_pv_transposed_heads])
+    _mut_pv_transposed_heads, _mut_decode_reads_compressed,
+    _mut_decode_position_restart])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     mutation(monkeypatch)
     caught = 0
