@@ -321,9 +321,10 @@ def run_gpu(args, sh):
             r = n % RING
             h.prefill_frame(dq[r], dk[r], dv[r], o, stream)
         g = torch.Generator(device="cpu").manual_seed(5)
-        tq = torch.randn((sh.streams, sh.layers, sh.q_heads, 1, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
-        tk = torch.randn((sh.streams, sh.layers, sh.kv_heads, 1, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
-        tv = torch.randn((sh.streams, sh.layers, sh.kv_heads, 1, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
+        tok = args.decode_tokens
+        tq = torch.randn((sh.streams, sh.layers, sh.q_heads, tok, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
+        tk = torch.randn((sh.streams, sh.layers, sh.kv_heads, tok, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
+        tv = torch.randn((sh.streams, sh.layers, sh.kv_heads, tok, sh.head_dim), generator=g).to(torch.bfloat16).to(dev)
         to = torch.empty_like(tq)
         for _ in range(3):
             h.decode(tq, tk, tv, to, stream)
@@ -340,9 +341,10 @@ def run_gpu(args, sh):
         h.check_device_status()
         dms = d0.elapsed_time(d1) / n_dec
         units = sh.streams * sh.layers * sh.kv_heads
-        rows = k0 + (n_dec + 1) / 2.0                       # mean D rows read per step
+        rows = k0 + tok * (n_dec + 1) / 2.0                 # mean D rows read per step
         dbytes = units * rows * sh.head_dim * 2 * 2
-        dec = {"tokens_per_s": 1000.0 / dms, "us_per_step": dms * 1000.0,
+        dec = {"tokens_per_s": tok * 1000.0 / dms, "us_per_step": dms * 1000.0,
+               "tokens_per_step": tok,
                "d_rows_per_kv_head": int(k0), "steps": n_dec,
                "roofline": {"bound": "hbm", "achieved": dbytes / (dms / 1000.0) / 1e9,
                             "peak": peaks["hbm"], "unit": "GB/s",
@@ -416,6 +418,7 @@ def main():
     ap.add_argument("--frames", type=int, default=0, help="frames per video (default: N of the workload)")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--decode-steps", type=int, default=20)
+    ap.add_argument("--decode-tokens", type=int, default=1)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -42,7 +42,7 @@ template <int N>
 struct DecLayout {
     static constexpr int CHUNK = 128 * 128;          // [128 rows][64 bf16], 128B-swizzled
     static constexpr int KV_TILE = 2 * CHUNK;        // one K or V tile (d = 128)
-    static constexpr int NS = 2;                     // K/V stages
+    static constexpr int NS = N <= 32 ? 3 : 2;       // K/V stages (as many as fit)
     static constexpr int NCHUNK = N * 128;           // [N rows][64 bf16]
     static constexpr int Q_TILE = 2 * NCHUNK;        // Q [N][128]
     static constexpr int P_TILE = 2 * NCHUNK;        // P^T [N][128 keys]
