@@ -52,6 +52,10 @@
 extern "C" {
 #endif
 
+/* ------------------------------------------------------ selection policy */
+#define STATEKV_SELECT_TOPB    0    /* Top-B by attention score (StateKV)    */
+#define STATEKV_SELECT_WINDOW  1    /* the B most recent tokens (ReKV-style)  */
+
 /* ---------------------------------------------------------------- status */
 #define STATEKV_OK              0
 #define STATEKV_E_INVALID_ARG  -1   /* null pointer, bad size, bad index      */
@@ -94,8 +98,15 @@ typedef struct statekv_handle statekv_handle;   /* opaque */
  *                 handle's lifetime (关键设计 3)
  *   rope_orig_ctx YaRN original context L_orig (> 0 when alpha != 1)
  *   position_offset virtual position of the first video token (>= 0)
- * Limits: G*T <= 65536 query rows per unit; B + T <= 24576; positions must
- * fit in int32.
+ *   select_policy STATEKV_SELECT_TOPB (the method, 关键设计 2) or
+ *                 STATEKV_SELECT_WINDOW: keep the B most recent tokens
+ *                 instead, the sliding-window baseline the page compares
+ *                 against (ReKV, R frames = B/T).  Full self-attention is
+ *                 budget >= max_frames*T with either policy (nothing is ever
+ *                 evicted).
+ * Limits: G*T <= 65536 query rows per unit; B + T <= 24576 unless
+ * B >= max_frames*T (no eviction: then only memory bounds the pool);
+ * positions must fit in int32.
  * Environment: STATEKV_ATTN_CLUSTER = 2 or 4, read by statekv_create (and by
  * statekv_attend_scores_static on every call), makes bf16 attention CTAs of
  * consecutive query tiles of one KV head share each K/V tile by TMA
@@ -118,6 +129,7 @@ typedef struct statekv_config {
     double  rope_alpha;
     int64_t rope_orig_ctx;
     int64_t position_offset;
+    int32_t select_policy;
 } statekv_config;
 
 /* Human-readable name of a status code (static storage, never NULL). */

@@ -51,6 +51,7 @@ class Config(C.Structure):
         ("dtype", C.c_int32), ("device", C.c_int32),
         ("rope_theta", C.c_double), ("rope_alpha", C.c_double),
         ("rope_orig_ctx", C.c_int64), ("position_offset", C.c_int64),
+        ("select_policy", C.c_int32),
     ]
 
 

@@ -16,6 +16,8 @@
 //   3. an MSB-first radix select (8 passes of 8 bits, shared histogram with
 //      warp-aggregated increments) finds the E-th smallest key, E = m - B;
 //      keys at or below it are evicted;
+//      (window policy, the sliding-window baseline: the key is the position,
+//      so the B most recent tokens are kept);
 //   4. slot reuse: the pool is [compressed slots 0..c) ; frame rows c..c+T).
 //      Evicted slots below B ("holes") are refilled by surviving rows at or
 //      above B ("movers"), paired in slot order; only those rows move
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
         int32_t p = j < c ? pos[j] : a.pos_base + (j - c);
         scores[j] = s;
         spos[j] = p;
-        keys[j] = cand_key(s, p);
+        if (m > B) keys[j] = a.window ? (uint64_t)(uint32_t)p << 32 : cand_key(s, p);
     }
     if (m <= B) {                               // state not full: keep all
         for (int j = c + tid; j < m; j += kThreads) pos[j] = a.pos_base + (j - c);
@@ -192,7 +194,8 @@ size_t select_smem_bytes(int slots, int T) {
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
-    size_t smem = select_smem_bytes(a.slots, a.T);
+    // a handle that never evicts never reaches the key buffer
+    size_t smem = a.never_evicts ? 0 : select_smem_bytes(a.slots, a.T);
     cudaError_t e = cudaFuncSetAttribute(select_kernel,
         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

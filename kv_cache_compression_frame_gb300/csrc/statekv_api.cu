@@ -135,7 +135,14 @@ int validate(const statekv_config* c) {
     if (c->head_dim != 64 && c->head_dim != 128) return STATEKV_E_UNSUPPORTED;
     int64_t G = c->num_q_heads / c->num_kv_heads;
     if (G * c->frame_tokens > 65536) return STATEKV_E_UNSUPPORTED;
-    if ((int64_t)c->budget + c->frame_tokens > kMaxSlots) return STATEKV_E_UNSUPPORTED;
+    if (c->select_policy != STATEKV_SELECT_TOPB && c->select_policy != STATEKV_SELECT_WINDOW)
+        return STATEKV_E_INVALID_ARG;
+    // selection keeps the pool's keys in shared memory; a handle whose budget
+    // covers every frame it can hold never selects (full self-attention)
+    const bool never_evicts = (int64_t)c->budget >= (int64_t)c->max_frames * c->frame_tokens;
+    if (!never_evicts && (int64_t)c->budget + c->frame_tokens > kMaxSlots)
+        return STATEKV_E_UNSUPPORTED;
+    if ((int64_t)c->budget + c->frame_tokens > (1LL << 24)) return STATEKV_E_UNSUPPORTED;
     if (c->position_offset + (int64_t)c->max_frames * c->frame_tokens > 0x7fffffffLL)
         return STATEKV_E_UNSUPPORTED;
     int64_t units = (int64_t)c->num_streams * c->num_layers * c->num_kv_heads;
@@ -231,6 +238,8 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     sa.c = cc; sa.T = T; sa.B = c.budget; sa.row_bytes = d * h->esize;
     sa.pos_base = (int32_t)p0;
     sa.inv_rows = (float)(1.0 / ((double)h->G * T));
+    sa.window = c.select_policy == STATEKV_SELECT_WINDOW;
+    sa.never_evicts = (int64_t)c.budget >= (int64_t)c.max_frames * T;
     e = timed(h, STATEKV_KERNEL_SELECT, st, [&] { return launch_select(sa, st); });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
 

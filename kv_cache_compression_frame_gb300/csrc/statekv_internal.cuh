@@ -63,6 +63,8 @@ struct SelectArgs {
     int32_t U, n_row_tiles, m_pad, slots, c, T, B, row_bytes;
     int32_t pos_base;     // virtual position of this frame's token 0
     float inv_rows;       // 1 / (G*T)
+    int32_t window;       // 1: keep the B most recent tokens instead of Top-B
+    int32_t never_evicts; // B >= every pool size this handle can reach
 };
 
 cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st);

@@ -17,6 +17,7 @@ import torch
 from . import _native as N
 
 _DTYPES = {"bf16": (N.BF16, torch.bfloat16), "f32": (N.F32, torch.float32)}
+_POLICIES = {"topb": 0, "window": 1}
 
 
 @dataclass
@@ -35,6 +36,7 @@ class StateKVConfig:
     rope_alpha: float = 1.0
     rope_orig_ctx: int = 0
     position_offset: int = 0
+    select_policy: str = "topb"      # "topb" (StateKV) or "window" (sliding-window baseline)
 
     @property
     def group(self) -> int:
@@ -56,8 +58,11 @@ class StateKVConfig:
     def _c(self, device: int) -> N.Config:
         if self.dtype not in _DTYPES:
             raise ValueError(f"dtype must be one of {list(_DTYPES)}")
+        if self.select_policy not in _POLICIES:
+            raise ValueError(f"select_policy must be one of {list(_POLICIES)}")
         d = asdict(self)
         d["dtype"] = _DTYPES[self.dtype][0]
+        d["select_policy"] = _POLICIES[self.select_policy]
         return N.Config(device=device, **d)
 
 

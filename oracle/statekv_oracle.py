@@ -174,6 +174,18 @@ def select_top_b(scores: np.ndarray, positions: np.ndarray,
     return keep[np.argsort(p[keep], kind="stable")]
 
 
+def select_window(positions: np.ndarray, budget: int) -> np.ndarray:
+    """The sliding-window baseline the page compares against (ReKV with a
+    window of R frames, compute-matched to B = R*T): keep the B most recent
+    candidates instead of the B highest-scoring ones.  Returns the kept
+    indices in ascending position."""
+    m = positions.shape[0]
+    if m <= budget:
+        return np.arange(m)
+    order = np.argsort(positions, kind="stable")
+    return np.sort(order[m - budget:])
+
+
 # ----------------------------------------------------- dual state (整体框架)
 @dataclass
 class UnitState:
@@ -204,14 +216,15 @@ class UnitState:
 def prefill_unit_frame(state: UnitState, q: np.ndarray, k: np.ndarray,
                        v: np.ndarray, n: int, *, budget: int,
                        omega: np.ndarray, scale: float, dtype: str,
-                       position_offset: int = 0):
+                       position_offset: int = 0, policy: str = "topb"):
     """One frame step of one (stream, layer, KV head).
 
     q: [G, T, d] pre-RoPE queries; k, v: [T, d] pre-RoPE keys and values.
     Steps, in the page's order of dependence:
       1. rotate Q and K at p = offset + nT + i (关键设计 3), round to storage;
       2. attend over [C_{n-1}; frame] (关键设计 1);
-      3. score every candidate of U_n and keep Top-B (关键设计 2);
+      3. score every candidate of U_n and keep Top-B (关键设计 2) -- or, for
+         the sliding-window baseline (policy "window"), the B most recent;
       4. C_n = kept rows; D_n = D_{n-1} ++ (K'_n, V_n) (关键设计 1).
     Mutates ``state``; returns (O [G,T,d], info dict).
     """
@@ -226,7 +239,8 @@ def prefill_unit_frame(state: UnitState, q: np.ndarray, k: np.ndarray,
     pool_pos = np.concatenate([state.comp_pos, pos_frame])
     O, P = attend_frame(q_rot, pool_k, pool_v, c, scale)
     s = importance_scores(P)
-    keep = select_top_b(s, pool_pos, budget)
+    keep = select_window(pool_pos, budget) if policy == "window" else \
+        select_top_b(s, pool_pos, budget)
     state.comp_k, state.comp_v, state.comp_pos = pool_k[keep], pool_v[keep], pool_pos[keep]
     state.det_k.append(k_rot)
     state.det_v.append(v)
@@ -293,7 +307,8 @@ class StateKVOracle:
             o, info = prefill_unit_frame(
                 st, q[s][l][h * G:(h + 1) * G], k[s][l][h], v[s][l][h], self.n,
                 budget=cfg.budget, omega=self.omega, scale=self.scale,
-                dtype=cfg.dtype, position_offset=self.offset)
+                dtype=cfg.dtype, position_offset=self.offset,
+                policy=getattr(cfg, "select_policy", "topb"))
             O[s, l, h * G:(h + 1) * G] = o
             if keep_info:
                 info.pop("P")

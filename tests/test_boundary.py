@@ -60,7 +60,9 @@ def _cfg(**kw):
     (dict(rope_alpha=4.0, rope_orig_ctx=0), N.E_INVALID_ARG),
     (dict(position_offset=-1), N.E_INVALID_ARG),
     (dict(head_dim=96), N.E_UNSUPPORTED),
-    (dict(budget=30000), N.E_UNSUPPORTED),
+    (dict(budget=30000, max_frames=4096), N.E_UNSUPPORTED),   # selects over > 24576 rows
+    (dict(budget=1 << 25), N.E_UNSUPPORTED),                    # no eviction, pool too large
+    (dict(select_policy=7), N.E_INVALID_ARG),
     (dict(max_frames=1 << 30, frame_tokens=256), N.E_UNSUPPORTED),
 ])
 def test_create_rejects_bad_config_before_device_work(lib, bad, want):

@@ -39,12 +39,14 @@ def _small(name, **kw) -> WorkloadShape:
 class Stepper:
     """Runs the CUDA path frame by frame and checks steps against the oracle."""
 
-    def __init__(self, shape: WorkloadShape, position_offset: int = 0):
+    def __init__(self, shape: WorkloadShape, position_offset: int = 0, policy: str = "topb"):
         from kv_cache_compression_frame_gb300 import StateKV, StateKVConfig
         self.sh = shape
         self.src = FrameSource(shape)
         self.offset = position_offset
-        self.h = StateKV(StateKVConfig.from_shape(shape, position_offset=position_offset))
+        self.policy = policy
+        self.h = StateKV(StateKVConfig.from_shape(shape, position_offset=position_offset,
+                                                  select_policy=policy))
         self.dev = self.h.device
         self.tdt = self.h.torch_dtype
         self.omega, ms = orc.rope_frequencies(shape.head_dim, shape.rope_theta,
@@ -110,7 +112,10 @@ class Stepper:
             nk, nv, npos, ncnt = h.compressed(s, l)
             assert ncnt == min(B, cnt + T)
             kept = npos[hk, :ncnt].cpu().numpy().astype(np.int64)
-            worst["swaps"] += check_selection(kept, s_ref, pool_pos, B, f"select {what}")
+            if self.policy == "window":          # the B most recent, exactly
+                np.testing.assert_array_equal(np.sort(kept), np.sort(pool_pos)[-ncnt:])
+            else:
+                worst["swaps"] += check_selection(kept, s_ref, pool_pos, B, f"select {what}")
             # slot-reuse gather: every live slot is a bit copy of its pool row
             where = {int(p): i for i, p in enumerate(pool_pos)}
             idx = torch.tensor([where[int(p)] for p in kept], dtype=torch.long)
@@ -330,3 +335,27 @@ def test_cluster_multicast_is_bit_identical(cluster, monkeypatch):
             assert a[3] == b[3]
             for x, y in zip(a[:3], b[:3]):
                 assert raw_equal(x.cpu(), y.cpu()), f"C frame {n}"
+
+
+def test_window_policy_keeps_the_most_recent_tokens():
+    """The sliding-window baseline on the same kernels: every step checked,
+    through the fill and well past it."""
+    sh = _small("window", q_heads=4, kv_heads=2, head_dim=128, frame_tokens=64,
+                budget=160, frames=6)
+    st = Stepper(sh, policy="window")
+    for n in range(sh.frames):
+        st.step(n)
+
+
+def test_full_attention_beyond_the_selection_limit():
+    """B >= max_frames*T never evicts: full causal self-attention over the
+    whole stream, with a pool (26,112 rows) larger than selection supports."""
+    sh = _small("fullsa", q_heads=2, kv_heads=1, head_dim=64, frame_tokens=256,
+                budget=102 * 256, frames=102)
+    st = Stepper(sh)
+    for n in range(sh.frames - 2):
+        st.run(n)
+    for n in (sh.frames - 2, sh.frames - 1):
+        st.step(n)
+    _, _, _, cnt = st.h.compressed(0, 0)
+    assert cnt == sh.frames * sh.frame_tokens

@@ -171,6 +171,42 @@ def check_decode_is_full_causal_over_the_stream(o=orc):
         assert state.detailed_k.shape[0] == N * T + 3
 
 
+def check_window_policy_is_a_sliding_window(o=orc):
+    """The sliding-window baseline (ReKV, compute-matched B): after every
+    frame C holds exactly the B most recent positions, and each frame query at
+    position p attends to the keys at positions [frame start - min(B, nT), p]
+    -- a contiguous range, checked by brute force."""
+    G, T, d, N, B = 2, 4, 8, 4, 6
+    theta = 1e4
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((N, G, T, d))
+    k = rng.standard_normal((N, T, d))
+    v = rng.standard_normal((N, T, d))
+    omega, ms = o.rope_frequencies(d, theta)
+    scale = o.logit_scale(d, ms)
+    pos_all = np.arange(N * T)
+    qr = [np.stack([_complex_rope(q[n, g], n * T + np.arange(T), theta) for g in range(G)])
+          .astype(np.float32).astype(np.float64) for n in range(N)]
+    kr = _complex_rope(k.reshape(N * T, d), pos_all, theta).astype(np.float32).astype(np.float64)
+    vv = v.reshape(N * T, d)
+    state = o.UnitState(d)
+    for n in range(N):
+        O, _ = o.prefill_unit_frame(state, q[n], k[n], v[n], n, budget=B, omega=omega,
+                                    scale=scale, dtype="f32", policy="window")
+        kept = min(B, (n + 1) * T)
+        np.testing.assert_array_equal(np.sort(state.comp_pos),
+                                      np.arange((n + 1) * T - kept, (n + 1) * T))
+        lo = n * T - min(B, n * T)
+        for i in range(T):
+            for g in range(G):
+                js = range(lo, n * T + i + 1)
+                logits = [float(np.dot(qr[n][g, i], kr[j])) / math.sqrt(d) for j in js]
+                mx = max(logits)
+                w = [math.exp(a - mx) for a in logits]
+                want = sum(wj / sum(w) * vv[j] for wj, j in zip(w, js))
+                np.testing.assert_allclose(O[g, i], want, rtol=0, atol=1e-12)
+
+
 def check_zero_budget_is_per_frame_causal(o=orc):
     """B = 0: no cross-frame state, so each frame is plain causal attention
     over its own tokens -- torch's scaled_dot_product_attention in fp64."""
@@ -232,6 +268,10 @@ def test_full_sa_special_case():
 
 def test_decode_matches_full_causal_over_the_stream():
     check_decode_is_full_causal_over_the_stream()
+
+
+def test_window_policy_is_a_sliding_window():
+    check_window_policy_is_a_sliding_window()
 
 
 def test_zero_budget_matches_sdpa():
@@ -435,6 +475,7 @@ def _mut_pv_transposed_heads(monkeypatch):
 
 _CHECKS = [check_golden_zero_keys, check_rope_complex,
            check_full_sa_when_budget_covers_all, check_decode_is_full_causal_over_the_stream,
+           check_window_policy_is_a_sliding_window,
            check_zero_budget_is_per_frame_causal, check_topb_rank_definition]
 
 
@@ -465,8 +506,15 @@ def _mut_decode_position_restart(monkeypatch):
     monkeypatch.setattr(orc, "decode_unit_tokens", bad)
 
 
+def _mut_window_keeps_oldest(monkeypatch):
+    def bad(positions, budget):
+        m = positions.shape[0]
+        return np.arange(m) if m <= budget else np.sort(np.argsort(positions)[:budget])
+    monkeypatch.setattr(orc, "select_window", bad)
+
+
 @pytest.mark.parametrize("mutation", [
-    _mut_mask_offbyone, _mut_score_visible_mean, _mut_tiebreak_high,
+    _mut_mask_offbyone, _mut_window_keeps_oldest, _mut_score_visible_mean, _mut_tiebreak_high,
     _mut_rope_sign, _mut_rope_freq_index, _mut_no_scale,
     _mut_pv_transposed_heads, _mut_decode_reads_compressed,
     _mut_decode_position_restart])
