@@ -19,6 +19,7 @@ video (independent streams; no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -181,7 +182,7 @@ def run_reference(args, sh):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * tot / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": sh.layers, "q_heads": sh.q_heads,
+        "config": {"workload": sh.name, "layers": sh.layers, "q_heads": sh.q_heads,
                    "kv_heads": sh.kv_heads, "head_dim": sh.head_dim, "T": sh.frame_tokens,
                    "B": sh.budget, "step": "one steady-state frame, all layers (bounded "
                                            "sample: 1 layer timed, scaled x28)"},
@@ -211,7 +212,8 @@ def run_gpu(args, sh):
     dv = [torch.from_numpy(r[2]).to(torch.bfloat16).to(dev) for r in ring]
     o = torch.empty_like(dq[0])
     # one frame of extra detailed-state rows: room for the text of the decode leg
-    h = StateKV(StateKVConfig.from_shape(sh, max_frames=frames + 1), device=local)
+    h = StateKV(StateKVConfig.from_shape(sh, max_frames=frames + 1,
+                                         select_policy=args.policy), device=local)
     stream = torch.cuda.current_stream(dev)
 
     def one_video():
@@ -376,12 +378,16 @@ def run_gpu(args, sh):
             "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "layers": sh.layers, "q_heads": sh.q_heads,
+            "config": {"workload": sh.name, "layers": sh.layers, "q_heads": sh.q_heads,
                        "kv_heads": sh.kv_heads, "head_dim": sh.head_dim,
                        "T": sh.frame_tokens, "B": sh.budget, "frames_per_step": frames,
+                       "policy": args.policy,
                        "rope_alpha": sh.rope_alpha, "parallelism": f"replicas x{ws}",
                        "l2": "inputs larger than L2 (16-frame ring, 117 MB compressed state)"},
             "tflops_algorithmic": step_flops * args.steps / (ms / 1000.0) / 1e12,
+            # attention pairs of one video relative to full self-attention
+            "attention_pairs_vs_full_sa": step_flops / sum(
+                dataclasses.replace(sh, budget=1 << 40).attention_flops(n) for n in range(frames)),
             "tflops_executed": 1.5 * step_flops * args.steps / (ms / 1000.0) / 1e12,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tc_sus"],
                          "unit": "TFLOP/s", "frac": achieved / peaks["tc_sus"],
@@ -422,9 +428,18 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--policy", default="topb", choices=["topb", "window"],
+                    help="selection: Top-B by score (the method) or the B most recent tokens "
+                         "(the sliding-window baseline)")
+    ap.add_argument("--budget", default="",
+                    help="override B; 'full' = full self-attention (B covers every frame)")
     args = ap.parse_args()
     from synth import SHAPES
     sh = SHAPES[args.workload]
+    if args.budget:
+        frames = args.frames or sh.frames
+        b = (frames + 1) * sh.frame_tokens if args.budget == "full" else int(args.budget)
+        sh = dataclasses.replace(sh, budget=b)
     if args.impl == "reference":
         run_reference(args, sh)
     else:
