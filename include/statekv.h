@@ -71,7 +71,8 @@ extern "C" {
 #define STATEKV_F32  1              /* fp32 storage and arithmetic            */
 
 /* kernels, for statekv_profile_read() */
-#define STATEKV_KERNEL_ROPE_TABLE 0 /* per-frame cos/sin table                */
+#define STATEKV_KERNEL_ROPE_TABLE 0 /* cos/sin table (computed once, at create: */
+                                    /* no launches inside a prefill)            */
 #define STATEKV_KERNEL_ROPE       1 /* RoPE at virtual positions + appends    */
 #define STATEKV_KERNEL_ATTENTION  2 /* two-sweep attention + key column sums  */
 #define STATEKV_KERNEL_SELECT     3 /* score finish, Top-B, slot-reuse gather */

@@ -6,15 +6,17 @@
 // run; 关键设计 1: the frame's K/V go to the detailed state D_n and join the
 // candidate pool next to the compressed state.
 //
-// Two kernels per frame:
-//  * rope_table: cos/sin of p*omega_k for the frame's T positions.  The angle
-//    reaches ~1.3e5 rad at 512 frames, where an fp32 product p*omega loses
-//    ~1e-2 rad, so the product and the reduction to [-pi, pi] are done in
-//    fp64 (T*d/2 angles per frame, shared by every head and layer);
+// Two kernels:
+//  * rope_table: cos/sin of p*omega_k for every position the detailed state
+//    can hold, once per handle (the frames' and the decoded text's).  The
+//    angle reaches ~1.3e5 rad at 512 frames, where an fp32 product p*omega
+//    loses ~1e-2 rad, so the product and the reduction to [-pi, pi] are done
+//    in fp64;
 //  * rope: one pass over Q, K and V of all (stream, layer, head) rows.
 //    Q' goes to scratch; K' and V go to the compressed pool after its c live
-//    slots and to D rows [nT, nT+T) (text tokens being decoded: D only).  16-byte vector loads/stores, rows of
-//    d/2 + d/2 pairs handled by d/(2*VEC) threads each.
+//    slots and to D rows [nT, nT+T) (text tokens being decoded: D only).
+//    16-byte vector loads/stores, rows of d/2 + d/2 pairs handled by
+//    d/(2*VEC) threads each.
 #include "statekv_internal.cuh"
 
 namespace statekv {
@@ -23,11 +25,11 @@ namespace {
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 
 __global__ void rope_table_kernel(RopeTableArgs a) {
-    int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    int total = a.T * a.half;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = (int64_t)a.T * a.half;
     if (idx >= total) return;
-    int i = idx / a.half;
-    int k = idx - i * a.half;
+    const int64_t i = idx / a.half;
+    const int k = (int)(idx - i * a.half);
     double ang = (double)(a.p0 + i) * a.omega[k];
     double turns = rint(ang * (1.0 / kTwoPi));
     double r = fma(-turns, kTwoPi, ang);          // in [-pi, pi] (+ rounding)
@@ -123,8 +125,9 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
 }  // namespace
 
 cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st) {
-    int total = a.T * a.half;
-    rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(a);
+    const int64_t blocks = ((int64_t)a.T * a.half + 255) / 256;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    rope_table_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

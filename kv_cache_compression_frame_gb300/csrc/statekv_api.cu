@@ -57,7 +57,7 @@ struct statekv_handle {
     float scale = 0.f, scale_log2 = 0.f;
 
     double* omega = nullptr;            // [d/2]
-    float2* cs = nullptr;               // [T][d/2]
+    float2* cs = nullptr;               // [det_pitch][d/2] cos/sin of every D row's position
     void* pool_k = nullptr; void* pool_v = nullptr;
     int32_t* pos = nullptr;
     void* det_k = nullptr; void* det_v = nullptr;
@@ -204,14 +204,11 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     const int64_t p0 = c.position_offset + h->n * T;
     cudaError_t e;
 
-    RopeTableArgs ta{h->omega, h->cs, p0, T, d / 2};
-    e = timed(h, STATEKV_KERNEL_ROPE_TABLE, st, [&] { return launch_rope_table(ta, st); });
-    if (e != cudaSuccess) return STATEKV_E_CUDA;
-
     RopeArgs ra{};
     ra.q = q; ra.k = k; ra.v = v;
     ra.q_rot = h->q_rot; ra.pool_k = h->pool_k; ra.pool_v = h->pool_v;
-    ra.det_k = h->det_k; ra.det_v = h->det_v; ra.cs = h->cs;
+    ra.det_k = h->det_k; ra.det_v = h->det_v;
+    ra.cs = h->cs + (size_t)h->n * T * (d / 2);          // rows of this frame's positions
     ra.rows_q = (int64_t)h->U * h->GT;
     ra.rows_kv = (int64_t)h->U * T;
     ra.T = T; ra.d = d; ra.slots = h->slots; ra.c = cc;
@@ -300,7 +297,7 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     const size_t row = (size_t)d * h->esize;
     bool ok = true;
     ok = ok && dalloc(h, &h->omega, sizeof(double) * d / 2);
-    ok = ok && dalloc(h, &h->cs, sizeof(float2) * (size_t)T * d / 2);
+    ok = ok && dalloc(h, &h->cs, sizeof(float2) * (size_t)h->det_pitch * d / 2);
     ok = ok && dalloc(h, &h->pool_k, (size_t)h->U * h->slots * row);
     ok = ok && dalloc(h, &h->pool_v, (size_t)h->U * h->slots * row);
     ok = ok && dalloc(h, &h->pos, sizeof(int32_t) * (size_t)h->U * h->slots);
@@ -323,6 +320,12 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     if (cudaMemcpy(h->omega, om.data(), sizeof(double) * om.size(), cudaMemcpyHostToDevice) !=
         cudaSuccess) {
         free_all(h); delete h; return STATEKV_E_CUDA;
+    }
+    // the rotation of every position D can hold (frames and decoded text),
+    // computed once: D row r is at virtual position position_offset + r
+    {
+        RopeTableArgs ta{h->omega, h->cs, c.position_offset, (int32_t)h->det_pitch, d / 2};
+        if (launch_rope_table(ta, nullptr) != cudaSuccess) { free_all(h); delete h; return STATEKV_E_CUDA; }
     }
     if (c.dtype == STATEKV_BF16 &&
         !make_tc_maps(&h->tc, h->pool_k, h->pool_v, d, h->slots, h->U, h->n_row_tiles)) {
@@ -476,13 +479,11 @@ int statekv_decode(statekv_handle* h, int32_t tokens, const void* q, const void*
         h->dec_items = items_max;
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
-    const int64_t p0 = c.position_offset + visible;
-    RopeTableArgs ta{h->omega, h->cs, p0, tokens, c.head_dim / 2};
-    if (launch_rope_table(ta, st) != cudaSuccess) return STATEKV_E_CUDA;
     RopeArgs ra{};
     ra.q = q; ra.k = k; ra.v = v;
     ra.q_rot = h->q_rot; ra.pool_k = nullptr; ra.pool_v = nullptr;
-    ra.det_k = h->det_k; ra.det_v = h->det_v; ra.cs = h->cs;
+    ra.det_k = h->det_k; ra.det_v = h->det_v;
+    ra.cs = h->cs + (size_t)visible * (c.head_dim / 2);
     ra.rows_q = (int64_t)h->U * R;
     ra.rows_kv = (int64_t)h->U * tokens;
     ra.T = tokens; ra.d = c.head_dim; ra.slots = h->slots; ra.c = 0;
