@@ -7,7 +7,8 @@
 //
 // One CTA per (stream, layer, KV head):
 //   1. s_j = (sum over query-row tiles of the column sums of P) / (G*T), in a
-//      fixed tile order (deterministic);
+//      fixed tile order (deterministic) -- unless the attention kernel's last
+//      CTA of the unit already did it (same order, same bits);
 //   2. every candidate gets the 64-bit key (float bits of s_j) << 32 |
 //      ~position: s_j >= 0, so the bit pattern orders like the value, and the
 //      complemented position makes the lower position win a tie.  Keys are
@@ -42,6 +43,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     __shared__ uint32_t warp_tot[2][kThreads / 32];
     __shared__ uint64_t s_prefix;
     __shared__ uint32_t s_rank;
+    __shared__ uint32_t s_unique;
 
     const int u = blockIdx.x;
     const int tid = threadIdx.x;
@@ -55,9 +57,14 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     float* scores = a.scores + (int64_t)u * a.m_pad;
     int32_t* spos = a.score_pos + (int64_t)u * a.m_pad;
     for (int j = tid; j < m; j += kThreads) {
-        float acc = 0.f;
-        for (int t = 0; t < a.n_row_tiles; ++t) acc += cs[(int64_t)t * a.m_pad + j];
-        float s = acc * a.inv_rows;
+        float s;
+        if (a.scores_done) {
+            s = scores[j];
+        } else {
+            float acc = 0.f;
+            for (int t = 0; t < a.n_row_tiles; ++t) acc += cs[(int64_t)t * a.m_pad + j];
+            s = acc * a.inv_rows;
+        }
         int32_t p = j < c ? pos[j] : a.pos_base + (j - c);
         scores[j] = s;
         spos[j] = p;
@@ -71,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
 
     // ---- 3. radix select of the E-th smallest key
     const uint32_t E = (uint32_t)(m - B);
-    if (tid == 0) { s_prefix = 0ull; s_rank = E; }
+    if (tid == 0) { s_prefix = 0ull; s_rank = E; s_unique = 0u; }
     for (int pass = 0; pass < 8; ++pass) {
         const int shift = 56 - 8 * pass;
         if (tid < 256) hist[tid] = 0u;
@@ -116,9 +123,20 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
                 }
                 s_prefix = prefix | ((uint64_t)(lane * 8 + b) << shift);
                 s_rank = rank - below;
+                s_unique = h[b] == 1u ? 1u : 0u;
             }
         }
         __syncthreads();
+        if (s_unique) {
+            // one key has this prefix: it is the E-th smallest; fetch it whole
+            // and skip the remaining digits (usually the position digits)
+            const uint64_t pre = s_prefix >> shift;
+            __syncthreads();
+            for (int j = tid; j < m; j += kThreads)
+                if ((keys[j] >> shift) == pre) s_prefix = keys[j];
+            __syncthreads();
+            break;
+        }
     }
     const uint64_t kappa = s_prefix;            // E-th smallest key: evict <= kappa
 

@@ -64,6 +64,7 @@ struct statekv_handle {
     void* q_rot = nullptr;
     float* colsum = nullptr;
     float* scores = nullptr;
+    uint32_t* unit_done = nullptr;      // [U] per-unit CTA counters of the attention kernel
     int32_t* score_pos = nullptr;
     uint32_t* err = nullptr;            // device status word
     void* stage_q = nullptr; void* stage_k = nullptr; void* stage_v = nullptr; void* stage_o = nullptr;
@@ -222,6 +223,9 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     aa.U = h->U; aa.GT = h->GT; aa.T = T; aa.d = d; aa.slots = h->slots; aa.c = cc;
     aa.m_pad = h->m_pad; aa.n_row_tiles = h->n_row_tiles;
     aa.scale = h->scale; aa.scale_log2 = h->scale_log2;
+    const bool tc = c.dtype == STATEKV_BF16;
+    if (tc) { aa.unit_done = h->unit_done; aa.scores = h->scores; }
+    aa.inv_rows = (float)(1.0 / ((double)h->G * T));
     e = timed(h, STATEKV_KERNEL_ATTENTION, st, [&] {
         return c.dtype == STATEKV_BF16 ? launch_attention_tc(aa, h->tc, st)
                                        : launch_attention_simt(aa, st);
@@ -236,6 +240,7 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     sa.pos_base = (int32_t)p0;
     sa.inv_rows = (float)(1.0 / ((double)h->G * T));
     sa.window = c.select_policy == STATEKV_SELECT_WINDOW;
+    sa.scores_done = tc;
     sa.never_evicts = (int64_t)c.budget >= (int64_t)c.max_frames * T;
     e = timed(h, STATEKV_KERNEL_SELECT, st, [&] { return launch_select(sa, st); });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
@@ -306,6 +311,7 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     ok = ok && dalloc(h, &h->q_rot, (size_t)h->U * h->GT * row);
     ok = ok && dalloc(h, &h->colsum, sizeof(float) * (size_t)h->U * h->n_row_tiles * h->m_pad);
     ok = ok && dalloc(h, &h->scores, sizeof(float) * (size_t)h->U * h->m_pad);
+    ok = ok && dalloc(h, &h->unit_done, sizeof(uint32_t) * (size_t)h->U);
     ok = ok && dalloc(h, &h->score_pos, sizeof(int32_t) * (size_t)h->U * h->m_pad);
     ok = ok && dalloc(h, &h->err, sizeof(uint32_t) * kErrWords);
     ok = ok && dalloc(h, &h->stage_q, h->q_bytes());
