@@ -51,13 +51,32 @@ def _peaks():
 
 
 def _dist():
+    """Replicas: one process per GPU (torchrun env).  Each rank streams its own
+    independent videos; the only collectives are the barriers around the
+    timed region and the max of the ranks' times.  NCCL on GPUs, gloo on a
+    host without them (the multi-process tests)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl"
-        dist.init_process_group(backend)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         return dist, int(os.environ["RANK"]), ws, int(os.environ.get("LOCAL_RANK", "0"))
     return None, 0, 1, 0
+
+
+def max_over_ranks(x: float, dist, device="cpu") -> float:
+    """The slowest rank's value (the job's time); x itself on one process."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(sh, rank: int) -> int:
+    """Each replica's synthetic videos: a seed of their own."""
+    return sh.seed + rank
 
 
 class ClockSampler:
@@ -167,8 +186,8 @@ def cpu_baseline(sh, layers: int = 3) -> dict:
 
 
 def run_reference(args, sh):
-    dist, rank, ws, _ = _dist()
-    if rank != 0:
+    # the oracle on the host cores: rank 0 alone under torchrun
+    if int(os.environ.get("RANK", "0")) != 0:
         return
     layers = 1
     for _ in range(args.warmup):
@@ -205,7 +224,7 @@ def run_gpu(args, sh):
     dev = torch.device("cuda", local)
     peaks = _peaks()
     frames = args.frames or sh.frames
-    src = FrameSource(sh, seed=sh.seed + rank)
+    src = FrameSource(sh, seed=replica_seed(sh, rank))
     ring = [src.frame(i) for i in range(RING)]
     dq = [torch.from_numpy(r[0]).to(torch.bfloat16).to(dev) for r in ring]
     dk = [torch.from_numpy(r[1]).to(torch.bfloat16).to(dev) for r in ring]
@@ -249,10 +268,7 @@ def run_gpu(args, sh):
     prof = h.profile_read()
     h.profile_enable(False)
     h.check_device_status()
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     total_frames = args.steps * frames * ws
     value = total_frames / (ms / 1000.0)
 
@@ -303,10 +319,7 @@ def run_gpu(args, sh):
         torch.cuda.synchronize()
         barrier()
         ems = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems, dist, dev)
         in_b = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * 2 * frames
         out_b = ho[0].numel() * 2 * frames
         e2e = {"value": args.e2e_steps * frames * ws / (ems / 1000.0), "unit": UNIT,
