@@ -52,6 +52,8 @@
 
 #include <cstdlib>
 
+#include <type_traits>
+
 #include "pipeline.cuh"
 
 namespace statekv {
@@ -415,8 +417,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_relaxed(sy.bar(L::B_S_READ + b));
             s_par ^= 1u << b;
-            const bool diag = t >= me.nfull;
             const int k0 = t * L::BN + colb;
+            // fully visible tiles and the few diagonal ones are separate
+            // instantiations: the per-element mask would otherwise be
+            // if-converted into every tile (16 % of the kernel's instructions)
+            auto rows1 = [&](auto diag_tag) {
+            constexpr bool diag = decltype(diag_tag)::value;
 #pragma unroll
             for (int ri = 0; ri < 4; ++ri) {
                 const uint32_t* r = (ri >> 1) ? r1 : r0;
@@ -427,7 +433,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     x[2 * rp] = __uint_as_float(r[4 * rp + 2 * sub]);
                     x[2 * rp + 1] = __uint_as_float(r[4 * rp + 2 * sub + 1]);
                 }
-                if (diag) {
+                if constexpr (diag) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         if (k0 + 8 * (e >> 1) + (e & 1) > lim[ri]) x[e] = -INFINITY;
@@ -448,6 +454,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 lrow[ri] = fmaf(lrow[ri], f, acc.x + acc.y);
                 mrow[ri] = mx;
             }
+            };
+            if (t >= me.nfull) rows1(std::true_type{});
+            else rows1(std::false_type{});
         }
         // combine: the 4 lanes of a row (bits 0, 1), then the 4 chunk warps
         auto merge = [&](float& m, float& l, float m2, float l2) {
@@ -502,10 +511,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_relaxed(sy.bar(L::B_S_READ + b));
             s_par ^= 1u << b;
-            const bool diag = t >= me.nfull;
             const int k0 = t * L::BN + colb;
             float c[8];                                // column partials: k = 2*rp + e
             uint32_t pk[2][8];
+            auto rows2 = [&](auto diag_tag) {
+            constexpr bool diag = decltype(diag_tag)::value;
 #pragma unroll
             for (int ri = 0; ri < 4; ++ri) {
                 const uint32_t* r = (ri >> 1) ? r1 : r0;
@@ -517,7 +527,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                      __uint_as_float(r[4 * rp + 2 * sub + 1])),
                                          make_float2(sc, sc), make_float2(nl, nl));
                     float2 p = make_float2(ptx::ex2_approx(z.x), ptx::ex2_approx(z.y));
-                    if (diag) {
+                    if constexpr (diag) {
                         if (k0 + 8 * rp > lim[ri]) p.x = 0.f;
                         if (k0 + 8 * rp + 1 > lim[ri]) p.y = 0.f;
                     }
@@ -529,6 +539,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     pk[ri >> 1][2 * rp + sub] = ptx::pack_bf16x2(p.x, p.y);
                 }
             }
+            };
+            if (t >= me.nfull) rows2(std::true_type{});
+            else rows2(std::false_type{});
             // P is free once PV(t-1) has completed (it was issued when P(t-1)
             // was complete, about one tile of softmax work ago)
             if (t > 0 && !sy.wait(L::B_P_FREE, p_par, kSitePEmpty)) {
