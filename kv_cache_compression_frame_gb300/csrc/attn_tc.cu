@@ -13,9 +13,11 @@
 // One CTA = one 128-row query tile of one (stream, layer, KV head); rows are
 // (g, i) pairs of the G query heads that share the KV head, g-major.  Two
 // sweeps over the 128-key tiles of the pool:
-//   sweep 1: S = Q K^T (tcgen05, fp32 in TMEM) -> per-thread running max and
-//            sum of exp2 over the thread's columns, combined across the
-//            row's threads at the end -> log-sum-exp per row;
+//   sweep 1: S = Q K^T (tcgen05, fp32 in TMEM) -> per thread and row, a sum
+//            of exp2 against a reference (the row's max when last raised:
+//            set by the first tile, raised only when a tile's sum passes
+//            2^32, so no max per tile), combined across the row's threads at
+//            the end -> log-sum-exp per row;
 //   sweep 2: S again, P = exp2(S*scale - lse) (final, normalised): column
 //            sums of fp32 P, and P -> bf16 into TMEM as the A operand of
 //            O += P V (tcgen05 with A in TMEM, V read MN-major from shared
@@ -402,9 +404,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
 
         // ---- sweep 1: per-thread running max / sum of exp2 over its columns
-        float mrow[4], lrow[4];
+        float mrow[4], lrow[4], nref[4];
 #pragma unroll
-        for (int ri = 0; ri < 4; ++ri) { mrow[ri] = -INFINITY; lrow[ri] = 0.f; }
+        for (int ri = 0; ri < 4; ++ri) { mrow[ri] = -INFINITY; lrow[ri] = 0.f; nref[ri] = 0.f; }
         for (int t = 0, b = 0; t < me.nt; ++t, b = (b == L::SB1 - 1) ? 0 : b + 1) {
             if (!sy.wait(L::B_S_FULL + b, (s_par >> b) & 1u, kSiteSFull)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -423,11 +425,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             // if-converted into every tile (16 % of the kernel's instructions)
             auto rows1 = [&](auto diag_tag) {
             constexpr bool diag = decltype(diag_tag)::value;
-#pragma unroll
-            for (int ri = 0; ri < 4; ++ri) {
+            // the row's 8 scores of this tile (masked ones -inf)
+            auto row_x = [&](int ri, float (&x)[8]) {
                 const uint32_t* r = (ri >> 1) ? r1 : r0;
                 const int sub = ri & 1;
-                float x[8];
 #pragma unroll
                 for (int rp = 0; rp < 4; ++rp) {
                     x[2 * rp] = __uint_as_float(r[4 * rp + 2 * sub]);
@@ -438,22 +439,50 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     for (int e = 0; e < 8; ++e)
                         if (k0 + 8 * (e >> 1) + (e & 1) > lim[ri]) x[e] = -INFINITY;
                 }
-                const float mx = ptx::max3(ptx::max3(x[0], x[1], x[2]),
-                                           ptx::max3(x[3], x[4], x[5]),
-                                           ptx::max3(x[6], x[7], mrow[ri]));
-                // branch-free online update; -inf rows stay at l = 0
-                const float nms = (mx == -INFINITY) ? 0.f : -mx * sc;
-                const float f = ptx::ex2_approx(fmaf(mrow[ri], sc, nms));
+            };
+            auto row_sum = [&](const float (&x)[8], float nref) -> float {
                 float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
                     float2 z = ptx::fma2(make_float2(x[e], x[e + 1]), make_float2(sc, sc),
-                                         make_float2(nms, nms));
+                                         make_float2(nref, nref));
                     acc = ptx::add2(acc, make_float2(ptx::ex2_approx(z.x), ptx::ex2_approx(z.y)));
                 }
-                lrow[ri] = fmaf(lrow[ri], f, acc.x + acc.y);
-                mrow[ri] = mx;
+                return acc.x + acc.y;
+            };
+            // each row sums exp2 against a reference (its running max as of the
+            // last time it was raised); the reference is raised only when a
+            // row is new or a tile's sum passes 2^32
+            float part[4];
+            bool raise = false;
+#pragma unroll
+            for (int ri = 0; ri < 4; ++ri) {
+                float x[8];
+                row_x(ri, x);
+                part[ri] = row_sum(x, nref[ri]);
+                raise |= !(part[ri] <= 0x1p32f) || mrow[ri] == -INFINITY;
             }
+            if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                for (int ri = 0; ri < 4; ++ri) {
+                    if (!(part[ri] <= 0x1p32f) || mrow[ri] == -INFINITY) {
+                        float x[8];
+                        row_x(ri, x);
+                        const float mx = ptx::max3(ptx::max3(x[0], x[1], x[2]),
+                                                   ptx::max3(x[3], x[4], x[5]),
+                                                   ptx::max3(x[6], x[7], mrow[ri]));
+                        if (mx != -INFINITY) {
+                            if (mrow[ri] != -INFINITY)
+                                lrow[ri] *= ptx::ex2_approx((mrow[ri] - mx) * sc);
+                            mrow[ri] = mx;
+                            nref[ri] = -mx * sc;
+                        }
+                        part[ri] = row_sum(x, nref[ri]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int ri = 0; ri < 4; ++ri) lrow[ri] += part[ri];
             };
             if (t >= me.nfull) rows1(std::true_type{});
             else rows1(std::false_type{});
