@@ -62,7 +62,10 @@ def check_rope(gpu: torch.Tensor, ref64: np.ndarray, x_in: np.ndarray, dtype: st
     rotation cancels, that absolute error is many ulps of a tiny result.
     Criterion: every element within 1 ulp (bf16) / 4 ulp (fp32) of the
     oracle, or within 2^-20 * pair magnitude (4x the fp32 bound); for bf16
-    fewer than 1e-3 of the elements may differ at all."""
+    at most 1e-3 of the elements, or 2 elements in an array too small for
+    that fraction to hold one, may differ at all (an fp32 result that sits
+    within its error bound of a bf16 rounding boundary rounds either way; a
+    wrong rounding mode or a dropped term moves far more)."""
     d = ulp_diff(gpu, ref64)
     err = np.abs(f64(gpu) - ref64)
     bound = 2.0 ** -20 * pair_magnitude(x_in)
@@ -70,9 +73,11 @@ def check_rope(gpu: torch.Tensor, ref64: np.ndarray, x_in: np.ndarray, dtype: st
     bad = (d > ulps) & (err > bound)
     assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond {ulps} ulp and the "
                            f"fp32 bound (max {d.max()} ulp, err/bound {float((err / bound).max()):.3g})")
-    frac = float((d > 0).mean())
+    n_diff = int((d > 0).sum())
+    frac = n_diff / max(d.size, 1)
     if dtype == "bf16":
-        assert frac < 1e-3, f"{what}: mismatch fraction {frac}"
+        assert n_diff <= max(2, int(1e-3 * d.size)), \
+            f"{what}: {n_diff} of {d.size} elements differ (fraction {frac})"
     return {"max_ulp": int(d.max()), "mismatch": frac}
 
 

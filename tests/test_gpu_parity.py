@@ -361,3 +361,17 @@ def test_full_attention_beyond_the_selection_limit():
         st.step(n)
     _, _, _, cnt = st.h.compressed(0, 0)
     assert cnt == sh.frames * sh.frame_tokens
+
+
+@pytest.mark.parametrize("head_dim,q_heads,kv_heads,T,B", [
+    (128, 6, 2, 1, 5),        # one token per frame, G = 3, budget below a tile
+    (64, 6, 2, 3, 7),         # odd T, odd B
+    (128, 3, 1, 129, 130),    # G*T = 387: a ragged fourth query tile, pool 259 rows
+    (64, 2, 2, 33, 0),        # G = 1, per-frame attention only
+])
+def test_odd_shapes_every_step(head_dim, q_heads, kv_heads, T, B):
+    sh = _small("odd", q_heads=q_heads, kv_heads=kv_heads, head_dim=head_dim,
+                frame_tokens=T, budget=B, frames=6)
+    st = Stepper(sh)
+    for n in range(sh.frames):
+        st.step(n)
