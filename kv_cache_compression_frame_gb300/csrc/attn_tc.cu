@@ -40,7 +40,9 @@
 // halves the MMA's share of the bandwidth.
 // TMEM (512 columns): Q (bf16 pairs) at 448..; sweep 1 -- three S buffers
 // (0, 128, 256); sweep 2 -- two S buffers (0, 128), O (256..), P (384..447,
-// bf16 pairs).  An S buffer is handed back to the MMA issuer as soon as its
+// bf16 pairs) in two 64-key halves, each with its own full/free barriers:
+// the 8 warps of one half refill it as soon as that half's PV products are
+// done, while the other half's still run.  An S buffer is handed back to the MMA issuer as soon as its
 // tile has been loaded into registers, so S(t+1) is computed while the
 // softmax works on S(t) and never waits for the signal that S(t) was read
 // (that arrive sits in the same per-SMSP queue as the softmax's ex2 burst
@@ -83,9 +85,9 @@ struct TcLayout {
     static constexpr int B_V_EMPTY = B_V_FULL + VS;
     static constexpr int B_S_FULL = B_V_EMPTY + VS;     // [SB1] S buffer computed
     static constexpr int B_S_READ = B_S_FULL + SB1;     // [SB1] S buffer loaded by all softmax warps
-    static constexpr int B_P_FULL = B_S_READ + SB1;     // P written by all softmax warps
-    static constexpr int B_P_FREE = B_P_FULL + 1;       // P consumed by PV
-    static constexpr int B_O_FULL = B_P_FREE + 1;
+    static constexpr int B_P_FULL = B_S_READ + SB1;     // [2] key half of P written by its 8 warps
+    static constexpr int B_P_FREE = B_P_FULL + 2;       // [2] key half of P consumed by PV
+    static constexpr int B_O_FULL = B_P_FREE + 2;
     static constexpr int B_DRAIN = B_O_FULL + 1;        // [2] each MMA issuer's teardown
     static constexpr int B_STAT = B_DRAIN + 2;          // row-statistics exchange
     static constexpr int NBAR = B_STAT + 1;
@@ -154,8 +156,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             ptx::mbar_init(sy.bar(L::B_S_FULL + b), 1);
             ptx::mbar_init(sy.bar(L::B_S_READ + b), L::SW);
         }
-        ptx::mbar_init(sy.bar(L::B_P_FULL), L::SW);
-        ptx::mbar_init(sy.bar(L::B_P_FREE), 1);
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(sy.bar(L::B_P_FULL + h), L::SW / 2);
+            ptx::mbar_init(sy.bar(L::B_P_FREE + h), 1);
+        }
         ptx::mbar_init(sy.bar(L::B_O_FULL), 1);
         ptx::mbar_init(sy.bar(L::B_DRAIN), 1);
         ptx::mbar_init(sy.bar(L::B_DRAIN + 1), 1);
@@ -308,23 +312,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int vs = t % L::VS, jv = t / L::VS;
             if (!(ok = sy.wait(L::B_V_FULL + vs, (uint32_t)(jv & 1), kSiteKvFull))) break;
             const bool mine = t < me.nt;
-            if (mine) {
-                // P(t) written by every softmax warp
-                if (!(ok = sy.wait(L::B_P_FULL, pv_par, kSitePFull))) break;
+            // each 64-key half of P(t) goes to the tensor pipe as soon as its
+            // 8 warps wrote it, and is handed back as soon as its 4 MMAs are
+            // done: the warps of one half refill it while the other half's
+            // products still run
+            for (int h = 0; mine && h < 2; ++h) {
+                if (!(ok = sy.wait(L::B_P_FULL + h, pv_par, kSitePFull))) break;
                 ptx::tc_fence_after();
-            }
-            if (ptx::elect_one()) {
-                if (mine) {
+                if (ptx::elect_one()) {
                     const uint32_t p_tmem = tmem + L::TM_P;
                     const uint32_t vb = vb0 + (uint32_t)vs * (L::TILE >> 4);
                     // MN-major V: LBO = distance between 64-wide d chunks,
                     // SBO = distance between 8-key row groups
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int ks = 4 * h + k4;
                         ptx::umma_ts_lh(tmem + L::TM_O, p_tmem + 8u * ks, vb + 128u * ks, v_hi,
                                         idesc_pv, (t | ks) ? 1u : 0u);
-                    ptx::umma_commit(sy.bar(L::B_P_FREE));
+                    }
+                    ptx::umma_commit(sy.bar(L::B_P_FREE + h));
                 }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (ptx::elect_one()) {
                 if (CS > 1) ptx::umma_commit_mc(sy.bar(L::B_V_EMPTY + vs), kMask);
                 else ptx::umma_commit(sy.bar(L::B_V_EMPTY + vs));
             }
@@ -363,6 +374,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             lim[ri] = r_unit < a.GT ? a.c + (r_unit % a.T) : -1;  // kk visible iff kk <= lim
         }
         const int colb = 32 * cq + 2 * (lane & 3);     // tile column of this thread's pair 0
+        const int ph = cq >> 1;                        // key half of P this warp writes
         float* colbuf = reinterpret_cast<float*>(base + L::OFF_COL);
         float2* statbuf = reinterpret_cast<float2*>(base + L::OFF_STAT);
         float* colsum = a.colsum + ((int64_t)u * n_rt + mt) * a.m_pad;
@@ -571,9 +583,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             };
             if (t >= me.nfull) rows2(std::true_type{});
             else rows2(std::false_type{});
-            // P is free once PV(t-1) has completed (it was issued when P(t-1)
-            // was complete, about one tile of softmax work ago)
-            if (t > 0 && !sy.wait(L::B_P_FREE, p_par, kSitePEmpty)) {
+            // this warp's half of P is free once its half of PV(t-1) has
+            // completed (issued when that half of P(t-1) was complete)
+            if (t > 0 && !sy.wait(L::B_P_FREE + ph, p_par, kSitePEmpty)) {
                 ok = false;
                 break;
             }
@@ -604,7 +616,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_P_FULL));
+            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_P_FULL + ph));
         }
         if (me.nt > 0)
             for (int kk = me.nt * L::BN + sw * 32 + lane; kk < a.m_pad; kk += 32 * L::SW)
