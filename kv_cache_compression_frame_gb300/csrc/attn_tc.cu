@@ -76,8 +76,9 @@ struct TcLayout {
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KS * TILE;
     static constexpr int OFF_COL = OFF_V + VS * TILE;   // float [NCOL][4 quarters][128]
-    static constexpr int OFF_STAT = OFF_COL + NCOL * 4 * 128 * 4;   // float2 [4 chunks][128 rows]
-    static constexpr int OFF_BAR = OFF_STAT + 4 * 128 * 8;
+    static constexpr int OFF_STAT = OFF_COL + NCOL * 4 * 128 * 4;   // float2 [16 threads][128 rows]
+    static constexpr int OFF_LSE = OFF_STAT + 16 * 128 * 8;         // float [128 rows]
+    static constexpr int OFF_BAR = OFF_LSE + 128 * 4;
     static constexpr int B_Q = 0;                       // Q in TMEM (all softmax warps)
     static constexpr int B_K_FULL = 1;
     static constexpr int B_K_EMPTY = B_K_FULL + KS;
@@ -89,13 +90,15 @@ struct TcLayout {
     static constexpr int B_P_FREE = B_P_FULL + 2;       // [2] key half of P consumed by PV
     static constexpr int B_O_FULL = B_P_FREE + 2;
     static constexpr int B_DRAIN = B_O_FULL + 1;        // [2] each MMA issuer's teardown
-    static constexpr int B_STAT = B_DRAIN + 2;          // row-statistics exchange
-    static constexpr int NBAR = B_STAT + 1;
+    static constexpr int B_STAT = B_DRAIN + 2;          // row statistics of every softmax thread stored
+    static constexpr int B_LSE = B_STAT + 1;            // lse of every row stored
+    static constexpr int NBAR = B_LSE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_O = 256, TM_P = 384, TM_Q = 448;
     static constexpr int THREADS = 96 + 32 * SW;
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 // Key range of one 128-row query tile: tiles [0, nt) hold a key visible to
@@ -164,6 +167,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::mbar_init(sy.bar(L::B_DRAIN), 1);
         ptx::mbar_init(sy.bar(L::B_DRAIN + 1), 1);
         ptx::mbar_init(sy.bar(L::B_STAT), L::SW);
+        ptx::mbar_init(sy.bar(L::B_LSE), 4);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -499,46 +503,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (t >= me.nfull) rows1(std::true_type{});
             else rows1(std::false_type{});
         }
-        // combine: the 4 lanes of a row (bits 0, 1), then the 4 chunk warps
-        auto merge = [&](float& m, float& l, float m2, float l2) {
-            const float mn = fmaxf(m, m2);
-            if (mn != -INFINITY) {
-                const float f1 = (m == -INFINITY) ? 0.f : ptx::ex2_approx((m - mn) * sc);
-                const float f2 = (m2 == -INFINITY) ? 0.f : ptx::ex2_approx((m2 - mn) * sc);
-                l = l * f1 + l2 * f2;
-            }
-            m = mn;
-        };
-#pragma unroll
-        for (int ri = 0; ri < 4; ++ri)
-#pragma unroll
-            for (int off = 1; off <= 2; off <<= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, mrow[ri], off);
-                const float l2 = __shfl_xor_sync(0xffffffffu, lrow[ri], off);
-                merge(mrow[ri], lrow[ri], m2, l2);
-            }
-        if ((lane & 3) == 0) {
+        // combine once per row: every thread stores its (reference, sum) for
+        // its 4 rows (16 threads hold parts of a row: 4 lanes x 4 chunk
+        // warps), then the 4 warps of chunk 0 merge one row per thread and
+        // publish its lse; merging in every thread instead repeats each
+        // row's merge 16 times right where no other work overlaps it
+        {
+            const int e = cq * 4 + (lane & 3);
 #pragma unroll
             for (int ri = 0; ri < 4; ++ri) {
                 const int row = q4 * 32 + 16 * (ri >> 1) + (lane >> 2) + 8 * (ri & 1);
-                statbuf[cq * 128 + row] = make_float2(mrow[ri], lrow[ri]);
+                statbuf[e * 128 + row] = make_float2(mrow[ri], lrow[ri]);
             }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_STAT));
-        float lse2[4];
-        if (!sy.wait(L::B_STAT, 0, kSiteCol)) ok = false;
+        float* lsebuf = reinterpret_cast<float*>(base + L::OFF_LSE);
+        if (cq == 0) {
+            if (!sy.wait(L::B_STAT, 0, kSiteCol)) ok = false;
+            const int row = q4 * 32 + lane;
+            float2 st[16];
+            float m = -INFINITY;
 #pragma unroll
-        for (int ri = 0; ri < 4; ++ri) {
-            const int row = q4 * 32 + 16 * (ri >> 1) + (lane >> 2) + 8 * (ri & 1);
-            float m = -INFINITY, l = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 st = statbuf[j * 128 + row];
-                merge(m, l, st.x, st.y);
+            for (int e = 0; e < 16; ++e) {
+                st[e] = statbuf[e * 128 + row];
+                m = fmaxf(m, st[e].x);
             }
-            lse2[ri] = (lim[ri] >= 0 && l > 0.f) ? fmaf(m, sc, log2f(l)) : INFINITY;
+            float l = 0.f;
+            if (m != -INFINITY) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (st[e].x != -INFINITY) l = fmaf(st[e].y, ptx::ex2_approx((st[e].x - m) * sc), l);
+            }
+            lsebuf[row] = (me.row0 + row < a.GT && l > 0.f) ? fmaf(m, sc, log2f(l)) : INFINITY;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_LSE));
         }
+        float lse2[4];
+        if (!sy.wait(L::B_LSE, 0, kSiteCol)) ok = false;
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri)
+            lse2[ri] = lsebuf[q4 * 32 + 16 * (ri >> 1) + (lane >> 2) + 8 * (ri & 1)];
 
         // ---- sweep 2: P, its column sums, P -> TMEM (bf16) for PV
         uint32_t p_par = 0;                            // parity of the P_FREE phase of PV(t-1)

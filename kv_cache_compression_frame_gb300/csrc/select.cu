@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
             s = acc * a.inv_rows;
         }
         int32_t p = j < c ? pos[j] : a.pos_base + (j - c);
-        scores[j] = s;
+        if (!a.scores_done) scores[j] = s;
         spos[j] = p;
         if (m > B) keys[j] = a.window ? (uint64_t)(uint32_t)p << 32 : cand_key(s, p);
     }
@@ -191,17 +191,34 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     const uint32_t np = s_pairs;
     for (uint32_t r = tid; r < np; r += kThreads) pos[holes[r]] = a.pos_base + (movers[r] - c);
 
-    // ---- row moves (K and V), 16-byte vectors
+    // ---- row moves (K and V), 16-byte vectors.  Holes are slots < B and
+    // movers slots >= B, so no row is both read and written: each thread
+    // issues all its loads (up to 4 vectors of K and of V) before its stores,
+    // one memory round trip instead of one per vector
+    constexpr int MV = 4;
     const int vpr = a.row_bytes / 16;
     const int64_t unit_bytes = (int64_t)a.slots * a.row_bytes;
     uint4* pk = reinterpret_cast<uint4*>((char*)a.pool_k + u * unit_bytes);
     uint4* pv = reinterpret_cast<uint4*>((char*)a.pool_v + u * unit_bytes);
     const int64_t total = (int64_t)np * vpr;
-    for (int64_t e = tid; e < total; e += kThreads) {
-        int r = (int)(e / vpr), w = (int)(e - (int64_t)r * vpr);
-        int64_t dst = (int64_t)holes[r] * vpr + w, src = (int64_t)movers[r] * vpr + w;
-        pk[dst] = pk[src];
-        pv[dst] = pv[src];
+    for (int64_t e0 = tid; e0 < total; e0 += MV * kThreads) {
+        uint4 vk[MV], vv[MV];
+        int64_t dst[MV];
+#pragma unroll
+        for (int q = 0; q < MV; ++q) {
+            const int64_t e = e0 + (int64_t)q * kThreads;
+            dst[q] = -1;
+            if (e < total) {
+                const int r = (int)(e / vpr), w = (int)(e - (int64_t)r * vpr);
+                const int64_t src = (int64_t)movers[r] * vpr + w;
+                dst[q] = (int64_t)holes[r] * vpr + w;
+                vk[q] = pk[src];
+                vv[q] = pv[src];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < MV; ++q)
+            if (dst[q] >= 0) { pk[dst[q]] = vk[q]; pv[dst[q]] = vv[q]; }
     }
 }
 
