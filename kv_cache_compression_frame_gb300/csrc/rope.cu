@@ -35,7 +35,7 @@ __global__ void rope_table_kernel(RopeTableArgs a) {
     double r = fma(-turns, kTwoPi, ang);          // in [-pi, pi] (+ rounding)
     float s, c;
     sincosf((float)r, &s, &c);
-    a.cs[idx] = make_float2(c, s);
+    a.cs[i * a.half + rope_cs_index(k, a.half, a.vec)] = make_float2(c, s);
 }
 
 template <typename E> struct Vec;
@@ -95,13 +95,18 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     Vec<E>::load(base + k0, x);
     Vec<E>::load(base + half + k0, y);
     if (kind != 2) {
-        const float2* cs = a.cs + (int64_t)i * half + k0;
+        // pairs 2p, 2p+1 of this thread: one 16-byte load (rope_cs_index)
+        const float4* cs = reinterpret_cast<const float4*>(a.cs + (int64_t)i * half);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            float2 t = cs[e];
+        for (int p = 0; p < VEC / 2; ++p) {
+            const float4 t = cs[p * tpr + j];
+            const int e = 2 * p;
             float xr = fmaf(x[e], t.x, -y[e] * t.y);
             float yr = fmaf(y[e], t.x, x[e] * t.y);
             x[e] = xr; y[e] = yr;
+            xr = fmaf(x[e + 1], t.z, -y[e + 1] * t.w);
+            yr = fmaf(y[e + 1], t.z, x[e + 1] * t.w);
+            x[e + 1] = xr; y[e + 1] = yr;
         }
     }
     uint4 lo = Vec<E>::pack(x), hi = Vec<E>::pack(y);

@@ -29,6 +29,7 @@ namespace statekv {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kHists = 16;                      // radix histograms, each shared by 2 warps
 
 __device__ __forceinline__ uint64_t cand_key(float s, int32_t pos) {
     return ((uint64_t)__float_as_uint(s) << 32) | (uint64_t)(0xffffffffu - (uint32_t)pos);
@@ -36,12 +37,15 @@ __device__ __forceinline__ uint64_t cand_key(float s, int32_t pos) {
 
 __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);          // [m]
-    int32_t* holes = reinterpret_cast<int32_t*>(keys + a.slots);     // [T]
-    int32_t* movers = holes + a.T;                                   // [T]
+    uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);          // [slots]
+    uint32_t* whist = reinterpret_cast<uint32_t*>(keys + a.slots);   // [kHists][256]
+    uint32_t* kept_bits = whist + kHists * 256;                      // [ceil(slots/32)]
+    // holes / movers [T] each reuse the key buffer once the keys are dead
+    int32_t* holes = reinterpret_cast<int32_t*>(keys);
+    int32_t* movers = holes + a.T;
     __shared__ uint32_t hist[256];
     __shared__ uint32_t warp_tot[2][kThreads / 32];
-    __shared__ uint64_t s_prefix;
+    __shared__ uint64_t s_prefix, s_and, s_or;
     __shared__ uint32_t s_rank;
     __shared__ uint32_t s_unique;
 
@@ -52,68 +56,122 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     const int m = c + T;
     int32_t* pos = a.pos + (int64_t)u * a.slots;
 
-    // ---- 1-2. scores, positions, keys
+    // ---- 1-2. scores, positions, keys (each thread's loads issued before
+    // its stores: the position and score buffers may alias as far as the
+    // compiler knows, which would otherwise serialise one round trip per key)
     const float* cs = a.colsum + (int64_t)u * a.n_row_tiles * a.m_pad;
     float* scores = a.scores + (int64_t)u * a.m_pad;
     int32_t* spos = a.score_pos + (int64_t)u * a.m_pad;
-    for (int j = tid; j < m; j += kThreads) {
-        float s;
-        if (a.scores_done) {
-            s = scores[j];
-        } else {
-            float acc = 0.f;
-            for (int t = 0; t < a.n_row_tiles; ++t) acc += cs[(int64_t)t * a.m_pad + j];
-            s = acc * a.inv_rows;
+    constexpr int KU = 4;
+    uint64_t k_and = ~0ull, k_or = 0ull;
+    for (int j0 = tid; j0 < m; j0 += KU * kThreads) {
+        float sv[KU];
+        int32_t pv[KU];
+#pragma unroll
+        for (int q = 0; q < KU; ++q) {
+            const int j = j0 + q * kThreads;
+            sv[q] = 0.f;
+            pv[q] = 0;
+            if (j < m) {
+                if (a.scores_done) {
+                    sv[q] = scores[j];
+                } else {
+                    float acc = 0.f;
+                    for (int t = 0; t < a.n_row_tiles; ++t) acc += cs[(int64_t)t * a.m_pad + j];
+                    sv[q] = acc * a.inv_rows;
+                }
+                pv[q] = j < c ? pos[j] : a.pos_base + (j - c);
+            }
         }
-        int32_t p = j < c ? pos[j] : a.pos_base + (j - c);
-        if (!a.scores_done) scores[j] = s;
-        spos[j] = p;
-        if (m > B) keys[j] = a.window ? (uint64_t)(uint32_t)p << 32 : cand_key(s, p);
+#pragma unroll
+        for (int q = 0; q < KU; ++q) {
+            const int j = j0 + q * kThreads;
+            if (j < m) {
+                if (!a.scores_done) scores[j] = sv[q];
+                spos[j] = pv[q];
+                if (m > B) {
+                    const uint64_t k = a.window ? (uint64_t)(uint32_t)pv[q] << 32 : cand_key(sv[q], pv[q]);
+                    keys[j] = k;
+                    k_and &= k;
+                    k_or |= k;
+                }
+            }
+        }
     }
     if (m <= B) {                               // state not full: keep all
         for (int j = c + tid; j < m; j += kThreads) pos[j] = a.pos_base + (j - c);
         return;
     }
-    __syncthreads();
 
-    // ---- 3. radix select of the E-th smallest key
+    // ---- 3. radix select of the E-th smallest key.  Bits every key shares
+    // are skipped (the score's sign and exponent bits usually): the first
+    // digit starts at the highest bit where keys differ.  Warps w and
+    // w + kHists share a histogram, so few increments of different warps
+    // collide on one address (with one histogram, every warp's increment
+    // of the one bucket all keys share serialised).
+    if (tid == 0) { s_and = ~0ull; s_or = 0ull; }
+    __syncthreads();
+    {
+        const uint32_t alo = __reduce_and_sync(0xffffffffu, (uint32_t)k_and);
+        const uint32_t ahi = __reduce_and_sync(0xffffffffu, (uint32_t)(k_and >> 32));
+        const uint32_t olo = __reduce_or_sync(0xffffffffu, (uint32_t)k_or);
+        const uint32_t ohi = __reduce_or_sync(0xffffffffu, (uint32_t)(k_or >> 32));
+        if (lane == 0) {
+            atomicAnd(reinterpret_cast<unsigned long long*>(&s_and), ((uint64_t)ahi << 32) | alo);
+            atomicOr(reinterpret_cast<unsigned long long*>(&s_or), ((uint64_t)ohi << 32) | olo);
+        }
+    }
     const uint32_t E = (uint32_t)(m - B);
-    if (tid == 0) { s_prefix = 0ull; s_rank = E; s_unique = 0u; }
-    for (int pass = 0; pass < 8; ++pass) {
-        const int shift = 56 - 8 * pass;
-        if (tid < 256) hist[tid] = 0u;
+    if (tid == 0) { s_rank = E; s_unique = 0u; }
+    __syncthreads();
+    const uint64_t diff = s_and ^ s_or;         // keys are distinct: diff != 0
+    const int top = 63 - __clzll((long long)diff);
+    if (tid == 0) s_prefix = top < 63 ? (s_and & (~0ull << (top + 1))) : 0ull;
+    int hi = top;                               // highest bit of the current digit
+    while (hi >= 0) {
+        const int width = min(8, hi + 1);
+        const int shift = hi + 1 - width;
+        const uint32_t dmask = (1u << width) - 1u;
+        for (int e = tid; e < kHists * 256; e += kThreads) whist[e] = 0u;
         __syncthreads();
         const uint64_t prefix = s_prefix;
+        uint32_t* wh = whist + (warp % kHists) * 256;
         for (int j0 = 0; j0 < m; j0 += kThreads) {
-            int j = j0 + tid;
+            const int j = j0 + tid;
             bool act = false;
             uint32_t dig = 0;
             if (j < m) {
-                uint64_t k = keys[j];
-                act = (pass == 0) || ((k >> (shift + 8)) == (prefix >> (shift + 8)));
-                dig = (uint32_t)(k >> shift) & 255u;
+                const uint64_t k = keys[j];
+                act = hi == 63 || (k >> (hi + 1)) == (prefix >> (hi + 1));
+                dig = (uint32_t)(k >> shift) & dmask;
             }
-            uint32_t amask = __ballot_sync(0xffffffffu, act);
+            const uint32_t amask = __ballot_sync(0xffffffffu, act);
             if (act) {
-                uint32_t peers = __match_any_sync(amask, dig);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
+                const uint32_t peers = __match_any_sync(amask, dig);
+                if (lane == __ffs(peers) - 1) atomicAdd(&wh[dig], (uint32_t)__popc(peers));
             }
         }
         __syncthreads();
+        if (tid < 256) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (int w = 0; w < kHists; ++w) acc += whist[w * 256 + tid];
+            hist[tid] = acc;
+        }
+        __syncthreads();
         if (warp == 0) {
-            uint32_t rank = s_rank;
+            const uint32_t rank = s_rank;
             uint32_t h[8], run = 0;
 #pragma unroll
             for (int e = 0; e < 8; ++e) { h[e] = hist[lane * 8 + e]; run += h[e]; }
             uint32_t incl = run;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
                 if (lane >= off) incl += y;
             }
-            uint32_t excl = incl - run;
-            bool mine = excl < rank && rank <= incl;
-            if (mine) {
+            const uint32_t excl = incl - run;
+            if (excl < rank && rank <= incl) {
                 uint32_t below = excl;
                 int b = 0;
 #pragma unroll
@@ -137,15 +195,25 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
             __syncthreads();
             break;
         }
+        hi -= width;
     }
     const uint64_t kappa = s_prefix;            // E-th smallest key: evict <= kappa
 
-    // ---- 4. holes (slots < B evicted) and movers (slots >= B kept), slot order
+    // ---- 4. holes (slots < B evicted) and movers (slots >= B kept), slot
+    // order: a kept-bit per candidate (coalesced key reads), then each thread
+    // counts and lists the candidates of its contiguous chunk from the bits
+    for (int j0 = 0; j0 < m; j0 += kThreads) {
+        const int j = j0 + tid;
+        const uint32_t bits = __ballot_sync(0xffffffffu, j < m && keys[j] > kappa);
+        if (lane == 0 && j0 + warp * 32 < m) kept_bits[(j0 >> 5) + warp] = bits;
+    }
+    __syncthreads();                            // keys dead: holes / movers may overwrite them
+    auto kept_at = [&](int j) -> bool { return (kept_bits[j >> 5] >> (j & 31)) & 1u; };
     const int per = (m + kThreads - 1) / kThreads;
     const int j0 = tid * per, j1 = min(j0 + per, m);
     uint32_t nh = 0, nm = 0;
     for (int j = j0; j < j1; ++j) {
-        bool kept = keys[j] > kappa;
+        const bool kept = kept_at(j);
         nh += (j < B && !kept);
         nm += (j >= B && kept);
     }
@@ -175,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     uint32_t oh = warp_tot[0][warp] + ih - nh;
     uint32_t om = warp_tot[1][warp] + im - nm;
     for (int j = j0; j < j1; ++j) {
-        bool kept = keys[j] > kappa;
+        const bool kept = kept_at(j);
         if (j < B && !kept) holes[oh++] = j;
         if (j >= B && kept) movers[om++] = j;
         // surviving frame rows that stay in place get their position
@@ -225,7 +293,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
 }  // namespace
 
 size_t select_smem_bytes(int slots, int T) {
-    return (size_t)slots * sizeof(uint64_t) + 2 * (size_t)T * sizeof(int32_t);
+    (void)T;                                    // holes / movers live in the key buffer
+    return (size_t)slots * sizeof(uint64_t) + (size_t)kHists * 256 * sizeof(uint32_t) +
+           (size_t)(slots + 31) / 32 * sizeof(uint32_t);
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {

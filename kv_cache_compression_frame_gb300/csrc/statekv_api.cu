@@ -141,7 +141,9 @@ int validate(const statekv_config* c) {
     // selection keeps the pool's keys in shared memory; a handle whose budget
     // covers every frame it can hold never selects (full self-attention)
     const bool never_evicts = (int64_t)c->budget >= (int64_t)c->max_frames * c->frame_tokens;
-    if (!never_evicts && (int64_t)c->budget + c->frame_tokens > kMaxSlots)
+    if (!never_evicts && ((int64_t)c->budget + c->frame_tokens > kMaxSlots ||
+                          select_smem_bytes(c->budget + c->frame_tokens, c->frame_tokens) >
+                              kSelectSmemMax))
         return STATEKV_E_UNSUPPORTED;
     if ((int64_t)c->budget + c->frame_tokens > (1LL << 24)) return STATEKV_E_UNSUPPORTED;
     if (c->position_offset + (int64_t)c->max_frames * c->frame_tokens > 0x7fffffffLL)
@@ -330,7 +332,8 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     // the rotation of every position D can hold (frames and decoded text),
     // computed once: D row r is at virtual position position_offset + r
     {
-        RopeTableArgs ta{h->omega, h->cs, c.position_offset, (int32_t)h->det_pitch, d / 2};
+        RopeTableArgs ta{h->omega, h->cs, c.position_offset, (int32_t)h->det_pitch, d / 2,
+                         c.dtype == STATEKV_BF16 ? 8 : 4};
         if (launch_rope_table(ta, nullptr) != cudaSuccess) { free_all(h); delete h; return STATEKV_E_CUDA; }
     }
     if (c.dtype == STATEKV_BF16 &&

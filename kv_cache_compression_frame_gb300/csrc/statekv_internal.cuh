@@ -27,7 +27,8 @@ struct RopeArgs {
     void* q_rot;                                   // [U*G*T][d]
     void* pool_k; void* pool_v;                    // [U][slots][d]
     void* det_k; void* det_v;                      // [U][det_pitch][d]
-    const float2* cs;                              // [T][d/2] (cos, sin)
+    const float2* cs;                              // [T][d/2] (cos, sin), vector-interleaved
+                                                   // rows (rope_cs_index)
     int64_t rows_q;      // S*L*Hq*T
     int64_t rows_kv;     // S*L*Hkv*T
     int32_t T, d, slots, c;
@@ -36,10 +37,21 @@ struct RopeArgs {
 
 struct RopeTableArgs {
     const double* omega;  // [d/2]
-    float2* cs;           // [T][d/2]
+    float2* cs;           // [T][d/2], rows vector-interleaved (rope_cs_index)
     int64_t p0;           // virtual position of token 0 of this frame
     int32_t T, half;
+    int32_t vec;          // pairs per RoPE thread: 8 (bf16) or 4 (fp32)
 };
+
+// Where pair k of a row sits in the (cos, sin) table.  A RoPE thread j
+// rotates pairs [j*vec, (j+1)*vec) of a row; the table keeps its pairs 2e and
+// 2e+1 side by side (one 16-byte load) and the same pair step of consecutive
+// threads in consecutive 16 bytes, so a warp's loads of one step are
+// contiguous instead of vec*8 bytes apart.
+__host__ __device__ __forceinline__ int rope_cs_index(int k, int half, int vec) {
+    const int tpr = half / vec, j = k / vec, e = k - j * vec;
+    return ((e >> 1) * tpr + j) * 2 + (e & 1);
+}
 
 struct AttnArgs {
     const void* q_rot;    // [U][GT][d]
@@ -116,6 +128,9 @@ constexpr int kSimtRowTile = 16;
 // Dynamic shared memory of the select kernel for B + T candidates.
 size_t select_smem_bytes(int slots, int T);
 constexpr int kMaxSlots = 24576;
+// dynamic shared memory the selection may take: the 227 KB a CTA can have
+// less what the kernel declares statically (histogram, scan, flags)
+constexpr size_t kSelectSmemMax = 227 * 1024 - 4096;
 
 }  // namespace statekv
 
