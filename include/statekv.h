@@ -296,8 +296,21 @@ int statekv_set_compressed(statekv_handle* h, int32_t s, int32_t layer,
  * every launch while enabled.  statekv_profile_read synchronises, then
  * returns for kernel id (STATEKV_KERNEL_*) the summed device milliseconds
  * and the number of launches since profiling was last enabled.
+ * statekv_profile_kernels restricts the bracketing to the kernels whose bit
+ * (1 << STATEKV_KERNEL_*) is set in mask (default: all).  An event recorded
+ * between two launches also ends the overlap of the second launch's start
+ * with the first one's end (below), so timing only the kernel of interest
+ * keeps the others' overlap.
+ *
+ * Overlap of consecutive launches within a frame sequence: the RoPE kernel
+ * of frame n+1 starts while the selection of frame n still runs (its query
+ * rows do not depend on it; its writes of the frame's keys into the pool
+ * wait for the selection to finish), and the attention kernel's set-up
+ * overlaps the RoPE kernel's end (programmatic dependent launch).  Any other
+ * operation on the stream between two calls separates them as usual.
  */
 int statekv_profile_enable(statekv_handle* h, int enable);
+int statekv_profile_kernels(statekv_handle* h, uint32_t mask);
 int statekv_profile_read(statekv_handle* h, int32_t kernel, double* total_ms,
                          int64_t* launches);
 

@@ -38,6 +38,7 @@ EXPORTS = (
     "statekv_reset", "statekv_check_device_status", "statekv_get_scores",
     "statekv_get_rotated_query", "statekv_set_frame_index",
     "statekv_set_compressed", "statekv_profile_enable", "statekv_profile_read",
+    "statekv_profile_kernels",
     "statekv_attend_scores_static", "statekv_decode", "statekv_text_tokens",
 )
 
@@ -99,6 +100,7 @@ def load() -> C.CDLL:
         "statekv_set_compressed": (C.c_int, [h, C.c_int32, C.c_int32, _P, _P, _P,
                                              C.c_int32, _P]),
         "statekv_profile_enable": (C.c_int, [h, C.c_int]),
+        "statekv_profile_kernels": (C.c_int, [h, C.c_uint32]),
         "statekv_profile_read": (C.c_int, [h, C.c_int32, C.POINTER(C.c_double),
                                            C.POINTER(C.c_int64)]),
         "statekv_attend_scores_static": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int32,

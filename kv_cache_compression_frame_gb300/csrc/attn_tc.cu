@@ -182,6 +182,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (CS > 1) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // set-up above may overlap the end of the RoPE kernel (programmatic
+    // dependent launch); every read and write of global memory comes after
+    ptx::dep_wait();
 
     const uint32_t sK = sbase + L::OFF_K;
     const uint32_t sV = sbase + L::OFF_V;
@@ -697,13 +700,15 @@ cudaError_t launch_tc(const AttnArgs& a, const TcMaps& m, cudaStream_t st) {
     cfg.blockDim = dim3(L::THREADS);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, CS>, m.k, m.v, a);
 }
 

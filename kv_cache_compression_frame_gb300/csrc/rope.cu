@@ -18,6 +18,7 @@
 //    16-byte vector loads/stores, rows of d/2 + d/2 pairs handled by
 //    d/(2*VEC) threads each.
 #include "statekv_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace statekv {
 namespace {
@@ -73,6 +74,9 @@ template <> struct Vec<float> {
 template <typename E>
 __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     constexpr int VEC = Vec<E>::N;
+    // the attention kernel that follows may set itself up meanwhile; it
+    // waits for this grid before it touches memory
+    ptx::dep_trigger();
     const int half = a.d / 2;
     const int tpr = half / VEC;                      // threads per row
     int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -117,14 +121,18 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
         return;
     }
     const int64_t unit = src_row / a.T;
+    E* det = (E*)(kind == 1 ? a.det_k : a.det_v) + (unit * a.det_pitch + a.det_row0 + i) * a.d;
+    *reinterpret_cast<uint4*>(det + k0) = lo;
+    *reinterpret_cast<uint4*>(det + half + k0) = hi;
     if (a.pool_k) {                                  // text tokens go to D only
+        // the previous frame's selection (possibly still running: this
+        // kernel may start early, see launch_rope) reads the pool's frame
+        // rows, which these stores replace
+        ptx::dep_wait();
         E* pool = (E*)(kind == 1 ? a.pool_k : a.pool_v) + (unit * a.slots + a.c + i) * a.d;
         *reinterpret_cast<uint4*>(pool + k0) = lo;
         *reinterpret_cast<uint4*>(pool + half + k0) = hi;
     }
-    E* det = (E*)(kind == 1 ? a.det_k : a.det_v) + (unit * a.det_pitch + a.det_row0 + i) * a.d;
-    *reinterpret_cast<uint4*>(det + k0) = lo;
-    *reinterpret_cast<uint4*>(det + half + k0) = hi;
 }
 
 }  // namespace
@@ -136,16 +144,29 @@ cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st) {
+// early: the kernel may start while the previous kernel of the stream (the
+// previous frame's selection, which triggers its dependents at its start)
+// still runs.  Safe because that selection started only after the previous
+// frame's attention ended, so Q' (read by that attention) may be rewritten
+// at once, and the pool rows the selection reads are written after
+// dep_wait().  Inputs q, k, v were written before the selection was queued
+// or by an operation between the two, which then orders them as usual.
+cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st, bool early) {
     int vec = dtype == STATEKV_BF16 ? 8 : 4;
     int64_t threads = (a.rows_q + 2 * a.rows_kv) * (a.d / 2 / vec);
     int64_t blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    if (dtype == STATEKV_BF16)
-        rope_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(a);
-    else
-        rope_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    if (dtype == STATEKV_BF16) return cudaLaunchKernelEx(&cfg, rope_kernel<__nv_bfloat16>, a);
+    return cudaLaunchKernelEx(&cfg, rope_kernel<float>, a);
 }
 
 }  // namespace statekv

@@ -24,6 +24,7 @@
 //      above B ("movers"), paired in slot order; only those rows move
 //      (<= T rows of K and V per unit instead of rewriting all B).
 #include "statekv_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace statekv {
 namespace {
@@ -49,6 +50,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     __shared__ uint32_t s_rank;
     __shared__ uint32_t s_unique;
 
+    // the next frame's RoPE kernel may start now (it waits for this grid
+    // before it writes the pool rows read here)
+    ptx::dep_trigger();
     const int u = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;

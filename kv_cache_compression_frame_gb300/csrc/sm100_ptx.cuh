@@ -82,6 +82,14 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel of the stream ends;
+// dep_wait() returns once that kernel has completed and its writes are
+// visible (at once for an ordinary launch), and dep_trigger() lets the next
+// kernel start early.
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 3-D tiled load into this CTA's shared memory, completing on an mbarrier
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m,
                                             uint32_t bar, int x, int y, int z) {

@@ -77,6 +77,7 @@ struct statekv_handle {
     TcMaps tc{};                        // TMA views for the bf16 attention kernel
 
     bool profiling = false;
+    uint32_t prof_mask = 0xffffffffu;   // kernels bracketed while profiling
     std::vector<PendingEvent> pending;
     std::vector<cudaEvent_t> spare;
     double prof_ms[STATEKV_NUM_KERNELS] = {0, 0, 0, 0};
@@ -184,7 +185,7 @@ cudaEvent_t take_event(statekv_handle* h) {
 // Runs one launch, bracketed by events when profiling.
 template <typename F>
 cudaError_t timed(statekv_handle* h, int kernel, cudaStream_t st, F&& launch) {
-    if (!h->profiling) return launch();
+    if (!h->profiling || !((h->prof_mask >> kernel) & 1u)) return launch();
     PendingEvent pe{kernel, take_event(h), take_event(h)};
     cudaEventRecord(pe.start, st);
     cudaError_t e = launch();
@@ -216,7 +217,7 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     ra.rows_kv = (int64_t)h->U * T;
     ra.T = T; ra.d = d; ra.slots = h->slots; ra.c = cc;
     ra.det_pitch = h->det_pitch; ra.det_row0 = h->n * T;
-    e = timed(h, STATEKV_KERNEL_ROPE, st, [&] { return launch_rope(ra, c.dtype, st); });
+    e = timed(h, STATEKV_KERNEL_ROPE, st, [&] { return launch_rope(ra, c.dtype, st, true); });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
 
     AttnArgs aa{};
@@ -497,7 +498,7 @@ int statekv_decode(statekv_handle* h, int32_t tokens, const void* q, const void*
     ra.rows_kv = (int64_t)h->U * tokens;
     ra.T = tokens; ra.d = c.head_dim; ra.slots = h->slots; ra.c = 0;
     ra.det_pitch = h->det_pitch; ra.det_row0 = visible;
-    if (launch_rope(ra, c.dtype, st) != cudaSuccess) return STATEKV_E_CUDA;
+    if (launch_rope(ra, c.dtype, st, false) != cudaSuccess) return STATEKV_E_CUDA;
     DecodeMaps maps;
     if (!make_decode_maps(&maps, h->q_rot, R, npad, h->det_k, h->det_v, h->det_pitch, h->U))
         return STATEKV_E_CUDA;
@@ -623,6 +624,12 @@ int statekv_profile_enable(statekv_handle* h, int enable) {
         h->pending.clear();
         for (int i = 0; i < STATEKV_NUM_KERNELS; ++i) { h->prof_ms[i] = 0; h->prof_n[i] = 0; }
     }
+    return STATEKV_OK;
+}
+
+int statekv_profile_kernels(statekv_handle* h, uint32_t mask) {
+    if (!h) return STATEKV_E_INVALID_ARG;
+    h->prof_mask = mask;
     return STATEKV_OK;
 }
 

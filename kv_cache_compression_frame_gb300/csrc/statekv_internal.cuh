@@ -85,7 +85,7 @@ struct SelectArgs {
 };
 
 cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st);
-cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st, bool early);
 // TMA views of the attention kernel's operands and the cluster size they
 // were encoded for (K/V boxes hold 128 / cs rows: each CTA of a cluster
 // loads that share of a tile and multicasts it).

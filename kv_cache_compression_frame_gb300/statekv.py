@@ -275,6 +275,17 @@ class StateKV:
     def profile_enable(self, on: bool = True) -> None:
         N.check(self._lib.statekv_profile_enable(self._h, int(on)), "statekv_profile_enable")
 
+    def profile_kernels(self, *names: str) -> None:
+        """Bracket only these kernels ("rope", "attention", "select", ...) with
+        events while profiling; no names = every kernel."""
+        mask = 0
+        for name in names:
+            if name not in N.KERNEL_NAMES:
+                raise ValueError(f"unknown kernel {name!r}: one of {N.KERNEL_NAMES}")
+            mask |= 1 << N.KERNEL_NAMES.index(name)
+        N.check(self._lib.statekv_profile_kernels(self._h, mask if names else 0xffffffff),
+                "statekv_profile_kernels")
+
     def profile_read(self) -> dict:
         """{kernel name: (total device ms, launches)} since profiling started."""
         out = {}
