@@ -82,6 +82,7 @@ def test_null_handle_and_pointers(lib):
     assert lib.statekv_set_frame_index(None, 0) == N.E_INVALID_ARG
     assert lib.statekv_check_device_status(None, None) == N.E_INVALID_ARG
     assert lib.statekv_profile_enable(None, 1) == N.E_INVALID_ARG
+    assert lib.statekv_profile_kernels(None, 1) == N.E_INVALID_ARG
     k = C.c_void_p()
     assert lib.statekv_get_rotated_query(None, C.byref(k)) == N.E_INVALID_ARG
     assert lib.statekv_get_compressed(None, 0, 0, None, None, None, None, None) == N.E_INVALID_ARG

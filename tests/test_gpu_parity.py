@@ -313,6 +313,20 @@ def test_profile_counts_every_launch():
     assert all(ms > 0 for ms, _ in prof.values()), prof
 
 
+def test_profile_kernels_brackets_only_the_chosen_kernel():
+    sh = _small("prof1", frames=3)
+    st = Stepper(sh)
+    st.h.profile_kernels("attention")
+    st.h.profile_enable(True)
+    for n in range(3):
+        st.run(n)
+    prof = st.h.profile_read()
+    assert prof["attention"][1] == 3 and prof["attention"][0] > 0, prof
+    assert all(cnt == 0 for k, (_, cnt) in prof.items() if k != "attention"), prof
+    with pytest.raises(ValueError):
+        st.h.profile_kernels("nope")
+
+
 @pytest.mark.parametrize("cluster", ["2", "4"])
 def test_cluster_multicast_is_bit_identical(cluster, monkeypatch):
     """K/V tiles shared by TMA multicast across a cluster of query-tile CTAs
@@ -375,3 +389,39 @@ def test_odd_shapes_every_step(head_dim, q_heads, kv_heads, T, B):
     st = Stepper(sh)
     for n in range(sh.frames):
         st.step(n)
+
+
+def test_overlapped_launches_match_serialised():
+    """Frames launched back to back (the next frame's RoPE starting while the
+    selection still runs, the attention set-up overlapping RoPE's end) give
+    the same bits as the same frames with events between every launch,
+    which serialise them.  Several units and query tiles, eviction every frame."""
+    from kv_cache_compression_frame_gb300 import StateKV, StateKVConfig
+    sh = _small("overlap", layers=4, q_heads=8, kv_heads=2, head_dim=128, frame_tokens=128,
+                budget=256, frames=10)
+    src = FrameSource(sh)
+    dev = torch.device("cuda:0")
+    frames = [tuple(torch.from_numpy(a).to(torch.bfloat16).to(dev) for a in src.frame(n))
+              for n in range(sh.frames)]
+    outs = {}
+    for mode in ("overlapped", "serialised"):
+        h = StateKV(StateKVConfig.from_shape(sh))
+        if mode == "serialised":
+            h.profile_enable(True)
+        os_ = [torch.empty_like(frames[0][0]) for _ in range(sh.frames)]
+        torch.cuda.synchronize()
+        for n, (q, k, v) in enumerate(frames):
+            h.prefill_frame(q, k, v, os_[n])
+        torch.cuda.synchronize()
+        h.check_device_status()
+        comp = [h.compressed(0, l) for l in range(sh.layers)]
+        outs[mode] = ([o.cpu() for o in os_],
+                      [(ck[:, :cnt].cpu(), cv[:, :cnt].cpu(), cp[:, :cnt].cpu()) for ck, cv, cp, cnt in comp])
+        h.close()
+    (oa, ca), (ob, cb) = outs["overlapped"], outs["serialised"]
+    for n in range(sh.frames):
+        assert torch.equal(oa[n].view(torch.int16), ob[n].view(torch.int16)), f"O of frame {n}"
+    for l in range(sh.layers):
+        for x, y in zip(ca[l], cb[l]):
+            assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                               y.view(torch.int16) if y.dtype == torch.bfloat16 else y), f"C of layer {l}"
