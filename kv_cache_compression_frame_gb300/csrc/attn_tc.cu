@@ -220,12 +220,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 return true;
             };
             // the order of first use: sweep 1 K(0..), sweep 2 K(0) K(1) then
-            // V(t) K(t+2) for every t
+            // K(t+2) V(t) for every t -- S(t+2) is issued as soon as the
+            // softmax has loaded S(t), PV(t) only once P(t) is written, so
+            // K(t+2) goes first; behind V(t), which waits for PV(t-2) to free
+            // its stage, it arrived just in time for S(t+2) to enter the
+            // tensor pipe ahead of PV(t) and delay it by a whole product
             for (int t = 0; ok && t < nt_load; ++t) ok = load(t, false);
             for (int t = 0; ok && t < min(2, nt_load); ++t) ok = load(t, false);
             for (int t = 0; ok && t < nt_load; ++t) {
-                ok = load(t, true);
-                if (ok && t + 2 < nt_load) ok = load(t + 2, false);
+                if (t + 2 < nt_load) ok = load(t + 2, false);
+                if (ok) ok = load(t, true);
             }
             // never leave a copy in flight into this CTA's shared memory: wait
             // for the last load of every stage (load n of stage s is number
