@@ -92,7 +92,8 @@ struct TcLayout {
     static constexpr int B_DRAIN = B_O_FULL + 1;        // [2] each MMA issuer's teardown
     static constexpr int B_STAT = B_DRAIN + 2;          // row statistics of every softmax thread stored
     static constexpr int B_LSE = B_STAT + 1;            // lse of every row stored
-    static constexpr int NBAR = B_LSE + 1;
+    static constexpr int B_S1_DONE = B_LSE + 1;         // the PV warp issued its sweep-1 S tiles
+    static constexpr int NBAR = B_S1_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
@@ -168,6 +169,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::mbar_init(sy.bar(L::B_DRAIN + 1), 1);
         ptx::mbar_init(sy.bar(L::B_STAT), L::SW);
         ptx::mbar_init(sy.bar(L::B_LSE), 4);
+        ptx::mbar_init(sy.bar(L::B_S1_DONE), 1);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -188,6 +190,50 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     const uint32_t sK = sbase + L::OFF_K;
     const uint32_t sV = sbase + L::OFF_V;
+
+    // S = Q K^T of K load kt into S buffer b, shared by the two issuer warps
+    // (warp 1; warp 2 in sweep 1, where it has no PV products to issue).
+    // Each issuer warp walks its schedule together and one elected lane
+    // issues each batch of MMAs and their commits; an issuing thread stalls
+    // while the tensor pipe's queue is full, and between batches its warp
+    // waits for issue slots on a sub-partition with four softmax warps, so
+    // two issuers halve that bookkeeping per tile in sweep 1.  prev_uses =
+    // earlier S products into buffer b: the buffer may be overwritten once
+    // every softmax warp loaded the last of them.  Phases follow from the
+    // tile indices, so the two warps need no shared state.
+    auto issue_s = [&](int kt, int b, bool needed, int prev_uses) -> bool {
+        constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false, false);
+        // a K step of 16 bf16 (32 bytes) adds 2 to the start-address field,
+        // a stage (TILE bytes) adds TILE >> 4; in TMEM a K step of Q is 8 columns
+        const uint32_t desc_hi = (uint32_t)(ptx::sdesc_sw128(0, 16, 1024) >> 32);
+        const uint32_t kb0 = (uint32_t)ptx::sdesc_sw128(sK, 16, 1024);
+        const int s = kt % L::KS, j = kt / L::KS;
+        if (!sy.wait(L::B_K_FULL + s, (uint32_t)(j & 1), kSiteKvFull)) return false;
+        ptx::tc_fence_after();
+        if (needed && prev_uses > 0) {
+            if (!sy.wait(L::B_S_READ + b, (uint32_t)((prev_uses - 1) & 1), kSiteSEmpty)) return false;
+            ptx::tc_fence_after();
+        }
+        if (ptx::elect_one()) {
+            if (needed) {
+                const uint32_t d = tmem + 128u * b;
+                const uint32_t kb = kb0 + (uint32_t)s * (L::TILE >> 4);
+#pragma unroll
+                for (int kc = 0; kc < L::KCH; ++kc)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        ptx::umma_ts_lh(d, tmem + L::TM_Q + 32u * kc + 8u * ks,
+                                        kb + kc * (L::CHUNK >> 4) + 2 * ks, desc_hi, idesc_qk,
+                                        (kc | ks) ? 1u : 0u);
+                ptx::umma_commit(sy.bar(L::B_S_FULL + b));
+            }
+            // the stage is free once every CTA of the cluster is done with it
+            if (CS > 1) ptx::umma_commit_mc(sy.bar(L::B_K_EMPTY + s), kMask);
+            else ptx::umma_commit(sy.bar(L::B_K_EMPTY + s));
+        }
+        __syncwarp();
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -241,68 +287,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- S = Q K^T issuer
-        // The whole warp walks the schedule (its values stay warp-uniform);
-        // one elected lane issues each batch of MMAs and their commits.  The
-        // PV products have an issuer of their own (warp 2): an issuing thread
-        // stalls while the tensor pipe's queue is full, and S(t+1) must not
-        // wait behind PV(t-1), which waits for the softmax.
-        constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false, false);
-        // descriptors are built once; a K step of 16 bf16 (32 bytes) adds 2
-        // to the start-address field, a stage (TILE bytes) adds TILE >> 4; in
-        // TMEM a K step of Q is 8 columns
-        const uint32_t desc_hi = (uint32_t)(ptx::sdesc_sw128(0, 16, 1024) >> 32);
-        const uint32_t kb0 = (uint32_t)ptx::sdesc_sw128(sK, 16, 1024);
-        const uint32_t tq = tmem + L::TM_Q;
-        int kt = 0;                                    // K tiles consumed
-        uint32_t s_used = 0, s_par = 0;                // per S buffer: issued yet / parity of last issue
-        // buffer b may be overwritten once every softmax warp loaded its tile
-        auto s_free = [&](int b) -> bool {
-            if (!((s_used >> b) & 1u)) return true;
-            if (!sy.wait(L::B_S_READ + b, (s_par >> b) & 1u, kSiteSEmpty)) return false;
-            ptx::tc_fence_after();
-            return true;
-        };
-        auto issue_s = [&](int b, bool needed) -> bool {
-            const int s = kt % L::KS, j = kt / L::KS;
-            if (!sy.wait(L::B_K_FULL + s, (uint32_t)(j & 1), kSiteKvFull)) return false;
-            ptx::tc_fence_after();
-            if (needed && !s_free(b)) return false;
-            if (ptx::elect_one()) {
-                if (needed) {
-                    const uint32_t d = tmem + 128u * b;
-                    const uint32_t kb = kb0 + (uint32_t)s * (L::TILE >> 4);
-#pragma unroll
-                    for (int kc = 0; kc < L::KCH; ++kc)
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            ptx::umma_ts_lh(d, tq + 32u * kc + 8u * ks,
-                                            kb + kc * (L::CHUNK >> 4) + 2 * ks, desc_hi, idesc_qk,
-                                            (kc | ks) ? 1u : 0u);
-                    ptx::umma_commit(sy.bar(L::B_S_FULL + b));
-                }
-                // the stage is free once every CTA of the cluster is done with it
-                if (CS > 1) ptx::umma_commit_mc(sy.bar(L::B_K_EMPTY + s), kMask);
-                else ptx::umma_commit(sy.bar(L::B_K_EMPTY + s));
-            }
-            __syncwarp();
-            if (needed) {
-                const uint32_t bit = 1u << b;
-                s_par ^= s_used & bit;
-                s_used |= bit;
-            }
-            ++kt;
-            return true;
-        };
         // Q is in TMEM once every softmax warp has stored its part
         bool ok = sy.wait(L::B_Q, 0, kSiteQFull);
         ptx::tc_fence_after();
-        // sweep 1: three S buffers in rotation
-        for (int t = 0, b = 0; ok && t < nt_load; ++t, b = (b == L::SB1 - 1) ? 0 : b + 1)
-            ok = issue_s(b, t < me.nt);
-        // sweep 2: S buffers 0 and 1; S(t+1) waits only for S(t-1) to have
-        // been loaded, so it is computed while the softmax works on S(t)
-        if (ok) ok = s_free(0) && s_free(1);
-        for (int t = 0; ok && t < nt_load; ++t) ok = issue_s(t & 1, t < me.nt);
+        // sweep 1: three S buffers in rotation; this warp issues the even
+        // tiles, the PV warp (idle until sweep 2) the odd ones
+        for (int t = 0; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < me.nt, t / L::SB1);
+        // sweep 2: S buffers 0 and 1; S(t+2) waits only for S(t) to have
+        // been loaded, so it is computed while the softmax works on S(t+1).
+        // This warp now also consumes the K stages and S buffers the PV warp
+        // used in sweep 1: it starts once that warp passed its last sweep-1
+        // waits, or a parity wait here could match a phase two back
+        if (ok) ok = sy.wait(L::B_S1_DONE, 0, kSiteSEmpty);
+        for (int t = 0; ok && t < nt_load; ++t) {
+            const int b = t & 1;
+            const int s1_uses = me.nt > b ? (me.nt - 1 - b) / L::SB1 + 1 : 0;
+            ok = issue_s(nt_load + t, b, t < me.nt, s1_uses + t / 2);
+        }
         // all MMAs complete before TMEM is released
         if (ptx::elect_one()) ptx::umma_commit(sy.bar(L::B_DRAIN));
         __syncwarp();
@@ -316,7 +317,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         uint32_t pv_par = 0;                           // parity of the next P_FULL phase
         const float* colbuf = reinterpret_cast<const float*>(base + L::OFF_COL);
         float* colsum = a.colsum + ((int64_t)u * n_rt + mt) * a.m_pad;
-        bool ok = true;
+        // sweep 1: the odd S tiles (warp 1 issues the even ones)
+        bool ok = sy.wait(L::B_Q, 0, kSiteQFull);
+        ptx::tc_fence_after();
+        for (int t = 1; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < me.nt, t / L::SB1);
+        if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S1_DONE));
         // O overlays sweep-1 S buffer 2: P(0) is written only after every
         // softmax warp finished sweep 1, so PV(0) waiting for P(0) is enough
         for (int t = 0; ok && t < nt_load; ++t) {
