@@ -14,8 +14,9 @@
 //      complemented position makes the lower position win a tie.  Keys are
 //      distinct, so "keep the B largest keys" is exactly Top-B with the tie
 //      rule;
-//   3. an MSB-first radix select (8 passes of 8 bits, shared histogram with
-//      warp-aggregated increments) finds the E-th smallest key, E = m - B;
+//   3. an MSB-first radix select (8-bit digits from the highest bit where
+//      keys differ; histograms shared by warp pairs) finds the E-th smallest
+//      key, E = m - B;
 //      keys at or below it are evicted;
 //      (window policy, the sliding-window baseline: the key is the position,
 //      so the B most recent tokens are kept);
@@ -46,7 +47,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     int32_t* movers = holes + a.T;
     __shared__ uint32_t hist[256];
     __shared__ uint32_t warp_tot[2][kThreads / 32];
-    __shared__ uint64_t s_prefix, s_and, s_or;
+    __shared__ uint64_t s_prefix, s_wand[kThreads / 32], s_wor[kThreads / 32];
     __shared__ uint32_t s_rank;
     __shared__ uint32_t s_unique;
 
@@ -113,32 +114,32 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     // w + kHists share a histogram, so few increments of different warps
     // collide on one address (with one histogram, every warp's increment
     // of the one bucket all keys share serialised).
-    if (tid == 0) { s_and = ~0ull; s_or = 0ull; }
-    __syncthreads();
+    // AND and OR of all keys: per warp, then every warp folds the warps'
+    // partials itself (no second barrier)
+    auto and64 = [](uint64_t v) {
+        return ((uint64_t)__reduce_and_sync(0xffffffffu, (uint32_t)(v >> 32)) << 32) |
+               __reduce_and_sync(0xffffffffu, (uint32_t)v);
+    };
+    auto or64 = [](uint64_t v) {
+        return ((uint64_t)__reduce_or_sync(0xffffffffu, (uint32_t)(v >> 32)) << 32) |
+               __reduce_or_sync(0xffffffffu, (uint32_t)v);
+    };
     {
-        const uint32_t alo = __reduce_and_sync(0xffffffffu, (uint32_t)k_and);
-        const uint32_t ahi = __reduce_and_sync(0xffffffffu, (uint32_t)(k_and >> 32));
-        const uint32_t olo = __reduce_or_sync(0xffffffffu, (uint32_t)k_or);
-        const uint32_t ohi = __reduce_or_sync(0xffffffffu, (uint32_t)(k_or >> 32));
-        if (lane == 0) {
-            atomicAnd(reinterpret_cast<unsigned long long*>(&s_and), ((uint64_t)ahi << 32) | alo);
-            atomicOr(reinterpret_cast<unsigned long long*>(&s_or), ((uint64_t)ohi << 32) | olo);
-        }
+        const uint64_t wa = and64(k_and), wo = or64(k_or);
+        if (lane == 0) { s_wand[warp] = wa; s_wor[warp] = wo; }
     }
-    const uint32_t E = (uint32_t)(m - B);
-    if (tid == 0) { s_rank = E; s_unique = 0u; }
+    for (int e = tid; e < kHists * 256; e += kThreads) whist[e] = 0u;
     __syncthreads();
-    const uint64_t diff = s_and ^ s_or;         // keys are distinct: diff != 0
+    const uint64_t k_all_and = and64(s_wand[lane]), k_all_or = or64(s_wor[lane]);
+    const uint64_t diff = k_all_and ^ k_all_or; // keys are distinct: diff != 0
     const int top = 63 - __clzll((long long)diff);
-    if (tid == 0) s_prefix = top < 63 ? (s_and & (~0ull << (top + 1))) : 0ull;
+    uint64_t prefix = top < 63 ? (k_all_and & (~0ull << (top + 1))) : 0ull;
+    uint32_t rank = (uint32_t)(m - B);          // E: the E-th smallest key is evicted last
     int hi = top;                               // highest bit of the current digit
     while (hi >= 0) {
         const int width = min(8, hi + 1);
         const int shift = hi + 1 - width;
         const uint32_t dmask = (1u << width) - 1u;
-        for (int e = tid; e < kHists * 256; e += kThreads) whist[e] = 0u;
-        __syncthreads();
-        const uint64_t prefix = s_prefix;
         uint32_t* wh = whist + (warp % kHists) * 256;
         for (int j0 = 0; j0 < m; j0 += kThreads) {
             const int j = j0 + tid;
@@ -149,11 +150,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
                 act = hi == 63 || (k >> (hi + 1)) == (prefix >> (hi + 1));
                 dig = (uint32_t)(k >> shift) & dmask;
             }
-            const uint32_t amask = __ballot_sync(0xffffffffu, act);
-            if (act) {
-                const uint32_t peers = __match_any_sync(amask, dig);
-                if (lane == __ffs(peers) - 1) atomicAdd(&wh[dig], (uint32_t)__popc(peers));
-            }
+            // one shared atomic per key: with the common high bits skipped the
+            // digits spread, and aggregating equal digits first (match_any)
+            // cost more than the few same-address conflicts it saves
+            if (act) atomicAdd(&wh[dig], 1u);
         }
         __syncthreads();
         if (tid < 256) {
@@ -164,7 +164,6 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
         }
         __syncthreads();
         if (warp == 0) {
-            const uint32_t rank = s_rank;
             uint32_t h[8], run = 0;
 #pragma unroll
             for (int e = 0; e < 8; ++e) { h[e] = hist[lane * 8 + e]; run += h[e]; }
@@ -187,8 +186,13 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
                 s_rank = rank - below;
                 s_unique = h[b] == 1u ? 1u : 0u;
             }
+        } else {
+            // the histograms are read; clear them for the next digit
+            for (int e = tid - 32; e < kHists * 256; e += kThreads - 32) whist[e] = 0u;
         }
         __syncthreads();
+        prefix = s_prefix;
+        rank = s_rank;
         if (s_unique) {
             // one key has this prefix: it is the E-th smallest; fetch it whole
             // and skip the remaining digits (usually the position digits)
