@@ -54,7 +54,9 @@
 // STATEKV_E_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM, exits.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdlib>
+#include <cstring>
 
 #include <type_traits>
 
@@ -78,7 +80,8 @@ struct TcLayout {
     static constexpr int OFF_COL = OFF_V + VS * TILE;   // float [NCOL][4 quarters][128]
     static constexpr int OFF_STAT = OFF_COL + NCOL * 4 * 128 * 4;   // float2 [16 threads][128 rows]
     static constexpr int OFF_LSE = OFF_STAT + 16 * 128 * 8;         // float [128 rows]
-    static constexpr int OFF_BAR = OFF_LSE + 128 * 4;
+    static constexpr int OFF_XLSE = OFF_LSE + 128 * 4;  // float [128 rows]: the other key half's lse
+    static constexpr int OFF_BAR = OFF_XLSE + 128 * 4;
     static constexpr int B_Q = 0;                       // Q in TMEM (all softmax warps)
     static constexpr int B_K_FULL = 1;
     static constexpr int B_K_EMPTY = B_K_FULL + KS;
@@ -93,7 +96,11 @@ struct TcLayout {
     static constexpr int B_STAT = B_DRAIN + 2;          // row statistics of every softmax thread stored
     static constexpr int B_LSE = B_STAT + 1;            // lse of every row stored
     static constexpr int B_S1_DONE = B_LSE + 1;         // the PV warp issued its sweep-1 S tiles
-    static constexpr int NBAR = B_S1_DONE + 1;
+    // split query tiles (two CTAs of a cluster, one key half each):
+    static constexpr int B_XLSE = B_S1_DONE + 1;        // the other half's lse partials arrived
+    static constexpr int B_XREADY = B_XLSE + 1;         // the other half's K stages may take our O
+    static constexpr int B_XO = B_XREADY + 1;           // the other half's O columns arrived
+    static constexpr int NBAR = B_XO + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
@@ -119,10 +126,18 @@ __device__ __forceinline__ TileRange tile_range(int row0, int GT, int T, int c) 
     return r;
 }
 
-template <int D, int CS>
+// SPLIT: the grid is clusters of two CTAs.  The first split_item0 query
+// tiles run whole, two per cluster (the CTAs do not interact); each later
+// tile is shared by the two CTAs of a cluster ("coop"), each taking one half
+// of its key tiles: they exchange the per-row lse partials after sweep 1 and
+// add each other's O columns at the end (through distributed shared memory).
+// The last, partial wave runs this way, so its tiles take about 60 % as long
+// on twice as many SMs, and start as soon as SMs free up in the wave before.
+template <int D, int CS, bool SPLIT>
 __global__ void __launch_bounds__(TcLayout<D>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, AttnArgs a) {
+    static_assert(!SPLIT || CS == 1, "split tiles do not multicast");
     using L = TcLayout<D>;
     constexpr int SLICE = 128 / CS;                     // K/V rows loaded by each CTA
     constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
@@ -134,13 +149,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rt = a.n_row_tiles;
     const int n_slots = (n_rt + CS - 1) / CS * CS;       // row tiles padded to whole clusters
-    const int u = blockIdx.x / n_slots;
-    const int mt = blockIdx.x - u * n_slots;
+    const int pair = (int)(blockIdx.x >> 1);
+    const bool coop = SPLIT && 2 * pair >= a.split_item0;
+    const int half = coop ? (int)ptx::cluster_ctarank() : 0;
+    const int item = coop ? a.split_item0 + (pair - a.split_item0 / 2) : (int)blockIdx.x;
+    const int u = item / n_slots;
+    const int mt = item - u * n_slots;
     const int rank = CS > 1 ? (int)ptx::cluster_ctarank() : 0;
     const TileRange me = tile_range(mt * 128, a.GT, a.T, a.c);
+    // this CTA's key tiles: [t0, t0 + nt_mine) of the tile's [0, me.nt)
+    const int t0 = coop && half ? me.nt / 2 : 0;
+    const int nt_mine = coop ? (half ? me.nt - me.nt / 2 : me.nt / 2) : me.nt;
     int nt_load = 0;                                    // key tiles the cluster streams
-    for (int r = 0; r < CS; ++r)
-        nt_load = max(nt_load, tile_range((mt - rank + r) * 128, a.GT, a.T, a.c).nt);
+    if (SPLIT) nt_load = nt_mine;
+    else
+        for (int r = 0; r < CS; ++r)
+            nt_load = max(nt_load, tile_range((mt - rank + r) * 128, a.GT, a.T, a.c).nt);
 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + L::OFF_MISC + 4);
@@ -170,6 +194,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::mbar_init(sy.bar(L::B_STAT), L::SW);
         ptx::mbar_init(sy.bar(L::B_LSE), 4);
         ptx::mbar_init(sy.bar(L::B_S1_DONE), 1);
+        ptx::mbar_init(sy.bar(L::B_XLSE), 128);                    // 4 warps x 32 lanes
+        ptx::mbar_init(sy.bar(L::B_XREADY), L::SW);
+        ptx::mbar_init(sy.bar(L::B_XO), (D / 64) * 128);          // the peer's senders, per lane
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -179,14 +206,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // peers multicast into this CTA's shared memory and barriers: all of
-    // them must be initialised first
-    if (CS > 1) ptx::cluster_sync();
+    // peers multicast into (or, split, write) this CTA's shared memory and
+    // arrive on its barriers: all of them must be initialised first
+    if (CS > 1 || coop) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // set-up above may overlap the end of the RoPE kernel (programmatic
     // dependent launch); every read and write of global memory comes after
     ptx::dep_wait();
+    // the split tail launch that may follow waits for this grid anyway
+    ptx::dep_trigger();
 
     const uint32_t sK = sbase + L::OFF_K;
     const uint32_t sV = sbase + L::OFF_V;
@@ -258,9 +287,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int kc = 0; kc < L::KCH; ++kc) {
                     if (CS > 1)
                         ptx::tma_load_3d_mc(dst + kc * L::CHUNK, map, fb, kc * 64,
-                                            t * L::BN + rank * SLICE, u, kMask);
+                                            (t0 + t) * L::BN + rank * SLICE, u, kMask);
                     else
-                        ptx::tma_load_3d(dst + kc * L::CHUNK, map, fb, kc * 64, t * L::BN, u);
+                        ptx::tma_load_3d(dst + kc * L::CHUNK, map, fb, kc * 64, (t0 + t) * L::BN, u);
                 }
                 if (is_v) ++vt; else ++kt;
                 return true;
@@ -292,7 +321,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::tc_fence_after();
         // sweep 1: three S buffers in rotation; this warp issues the even
         // tiles, the PV warp (idle until sweep 2) the odd ones
-        for (int t = 0; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < me.nt, t / L::SB1);
+        for (int t = 0; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < nt_mine, t / L::SB1);
         // sweep 2: S buffers 0 and 1; S(t+2) waits only for S(t) to have
         // been loaded, so it is computed while the softmax works on S(t+1).
         // This warp now also consumes the K stages and S buffers the PV warp
@@ -301,8 +330,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (ok) ok = sy.wait(L::B_S1_DONE, 0, kSiteSEmpty);
         for (int t = 0; ok && t < nt_load; ++t) {
             const int b = t & 1;
-            const int s1_uses = me.nt > b ? (me.nt - 1 - b) / L::SB1 + 1 : 0;
-            ok = issue_s(nt_load + t, b, t < me.nt, s1_uses + t / 2);
+            const int s1_uses = nt_mine > b ? (nt_mine - 1 - b) / L::SB1 + 1 : 0;
+            ok = issue_s(nt_load + t, b, t < nt_mine, s1_uses + t / 2);
         }
         // all MMAs complete before TMEM is released
         if (ptx::elect_one()) ptx::umma_commit(sy.bar(L::B_DRAIN));
@@ -320,14 +349,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         // sweep 1: the odd S tiles (warp 1 issues the even ones)
         bool ok = sy.wait(L::B_Q, 0, kSiteQFull);
         ptx::tc_fence_after();
-        for (int t = 1; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < me.nt, t / L::SB1);
+        for (int t = 1; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < nt_mine, t / L::SB1);
         if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S1_DONE));
         // O overlays sweep-1 S buffer 2: P(0) is written only after every
         // softmax warp finished sweep 1, so PV(0) waiting for P(0) is enough
         for (int t = 0; ok && t < nt_load; ++t) {
             const int vs = t % L::VS, jv = t / L::VS;
             if (!(ok = sy.wait(L::B_V_FULL + vs, (uint32_t)(jv & 1), kSiteKvFull))) break;
-            const bool mine = t < me.nt;
+            const bool mine = t < nt_mine;
             // each 64-key half of P(t) goes to the tensor pipe as soon as its
             // 8 warps wrote it, and is handed back as soon as its 4 MMAs are
             // done: the warps of one half refill it while the other half's
@@ -363,7 +392,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int e = 32 * j + lane;
-                    colsum[t * L::BN + e] = cb[e] + cb[128 + e] + cb[256 + e] + cb[384 + e];
+                    colsum[(t0 + t) * L::BN + e] = cb[e] + cb[128 + e] + cb[256 + e] + cb[384 + e];
                 }
             }
         }
@@ -435,7 +464,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         float mrow[4], lrow[4], nref[4];
 #pragma unroll
         for (int ri = 0; ri < 4; ++ri) { mrow[ri] = -INFINITY; lrow[ri] = 0.f; nref[ri] = 0.f; }
-        for (int t = 0, b = 0; t < me.nt; ++t, b = (b == L::SB1 - 1) ? 0 : b + 1) {
+        for (int t = 0, b = 0; t < nt_mine; ++t, b = (b == L::SB1 - 1) ? 0 : b + 1) {
             if (!sy.wait(L::B_S_FULL + b, (s_par >> b) & 1u, kSiteSFull)) { ok = false; break; }
             ptx::tc_fence_after();
             uint32_t r0[16], r1[16];
@@ -447,7 +476,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_relaxed(sy.bar(L::B_S_READ + b));
             s_par ^= 1u << b;
-            const int k0 = t * L::BN + colb;
+            const int k0 = (t0 + t) * L::BN + colb;
             // fully visible tiles and the few diagonal ones are separate
             // instantiations: the per-element mask would otherwise be
             // if-converted into every tile (16 % of the kernel's instructions)
@@ -512,7 +541,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
             for (int ri = 0; ri < 4; ++ri) lrow[ri] += part[ri];
             };
-            if (t >= me.nfull) rows1(std::true_type{});
+            if (t0 + t >= me.nfull) rows1(std::true_type{});
             else rows1(std::false_type{});
         }
         // combine once per row: every thread stores its (reference, sum) for
@@ -547,7 +576,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int e = 0; e < 16; ++e)
                     if (st[e].x != -INFINITY) l = fmaf(st[e].y, ptx::ex2_approx((st[e].x - m) * sc), l);
             }
-            lsebuf[row] = (me.row0 + row < a.GT && l > 0.f) ? fmaf(m, sc, log2f(l)) : INFINITY;
+            float lse = (me.row0 + row < a.GT && l > 0.f) ? fmaf(m, sc, log2f(l)) : INFINITY;
+            if (SPLIT && coop) {
+                // the row's lse over this CTA's key half (-inf: no key), sent
+                // to the other half; both combine the two partials
+                const float part = l > 0.f ? fmaf(m, sc, log2f(l)) : -INFINITY;
+                const uint32_t peer = (uint32_t)(half ^ 1);
+                ptx::st_cluster_f32(ptx::cluster_map(sbase + L::OFF_XLSE + 4u * row, peer), part);
+                ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XLSE), peer));
+                if (!sy.wait_cluster(L::B_XLSE, 0, kSiteCol)) ok = false;
+                const float other = reinterpret_cast<const float*>(base + L::OFF_XLSE)[row];
+                const float mx = fmaxf(part, other);
+                lse = (me.row0 + row < a.GT && mx != -INFINITY)
+                          ? mx + log2f(exp2f(part - mx) + exp2f(other - mx))
+                          : INFINITY;
+            }
+            lsebuf[row] = lse;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_LSE));
         }
@@ -559,7 +603,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
         // ---- sweep 2: P, its column sums, P -> TMEM (bf16) for PV
         uint32_t p_par = 0;                            // parity of the P_FREE phase of PV(t-1)
-        for (int t = 0, slot = 0; ok && t < me.nt; ++t, slot = (slot == L::NCOL - 1) ? 0 : slot + 1) {
+        for (int t = 0, slot = 0; ok && t < nt_mine; ++t, slot = (slot == L::NCOL - 1) ? 0 : slot + 1) {
             const int b = t & 1;
             if (!sy.wait(L::B_S_FULL + b, (s_par >> b) & 1u, kSiteSFull)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -569,7 +613,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_relaxed(sy.bar(L::B_S_READ + b));
             s_par ^= 1u << b;
-            const int k0 = t * L::BN + colb;
+            const int k0 = (t0 + t) * L::BN + colb;
             float c[8];                                // column partials: k = 2*rp + e
             uint32_t pk[2][8];
             auto rows2 = [&](auto diag_tag) {
@@ -598,7 +642,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             }
             };
-            if (t >= me.nfull) rows2(std::true_type{});
+            if (t0 + t >= me.nfull) rows2(std::true_type{});
             else rows2(std::false_type{});
             // this warp's half of P is free once its half of PV(t-1) has
             // completed (issued when that half of P(t-1) was complete)
@@ -635,12 +679,66 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_P_FULL + ph));
         }
-        if (me.nt > 0)
+        if (SPLIT && coop) {
+            // this CTA's key tiles are consumed: the other half may put its
+            // O columns into our K stages
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XREADY), (uint32_t)(half ^ 1)));
+        }
+        if (me.nt > 0 && (!coop || half == 1))         // the half holding the last tiles
             for (int kk = me.nt * L::BN + sw * 32 + lane; kk < a.m_pad; kk += 32 * L::SW)
                 colsum[kk] = 0.f;
 
         // ---- output rows: quarter q4, 32 columns per warp
-        if (me.nt > 0 && ok && cq < D / 32 && sy.wait(L::B_O_FULL, 0, kSiteOFull)) {
+        if (SPLIT && coop) {
+            // each half outputs D/2 columns: it adds the other half's partial
+            // O of them (stored column-major into its K stage 0, so a warp's
+            // 32 lanes = 32 rows write consecutive words) to its own
+            if (cq < D / 32) {
+                const int owner = (cq * 2) / (D / 32);
+                const int c0 = 32 * cq - owner * (D / 2);
+                const int row = q4 * 32 + lane;
+                float v[32];
+                bool have = false;
+                if (ok && nt_mine > 0 && sy.wait(L::B_O_FULL, 0, kSiteOFull)) {
+                    ptx::tc_fence_after();
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(tmem + L::TM_O + lane_h0 + 32 * cq, r);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    have = true;
+                }
+                if (!have) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;   // no key tiles: no mass
+                }
+                const uint32_t peer = (uint32_t)(half ^ 1);
+                if (owner != half) {
+                    if (sy.wait_cluster(L::B_XREADY, 0, kSiteCol)) {
+                        const uint32_t dst = ptx::cluster_map(sK, peer);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            ptx::st_cluster_f32(dst + 4u * (uint32_t)((c0 + j) * 128 + row), v[j]);
+                    }
+                    ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XO), peer));
+                } else if (sy.wait_cluster(L::B_XO, 0, kSiteCol) && me.row0 + row < a.GT) {
+                    const float* xo = reinterpret_cast<const float*>(base + L::OFF_K);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += xo[(c0 + j) * 128 + row];
+                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                         ((int64_t)u * a.GT + me.row0 + row) * D + 32 * cq;
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) wv[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                    uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
+                }
+            }
+        } else if (me.nt > 0 && ok && cq < D / 32 && sy.wait(L::B_O_FULL, 0, kSiteOFull)) {
             ptx::tc_fence_after();
             const int r_unit = me.row0 + q4 * 32 + lane;
             uint32_t r[32];
@@ -662,10 +760,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::tc_fence_before();
     }
 
+    // a split pair counts once, by half 0, after half 1's partials are out
+    if (coop) __threadfence();
     __syncthreads();
     // no CTA leaves while a peer may still multicast into it or arrive on
     // its barriers (every role above has drained its own traffic)
-    if (CS > 1) ptx::cluster_sync();
+    if (CS > 1 || coop) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, L::TMEM_COLS);
@@ -673,7 +773,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     // ---- scores (关键设计 2): the last of the unit's query-tile CTAs to
     // finish sums every tile's column partials in tile order (the fixed
     // order keeps s_j bit-reproducible) while other units still run
-    if (a.unit_done != nullptr && mt < n_rt) {
+    if (a.unit_done != nullptr && mt < n_rt && (!coop || half == 0)) {
         uint32_t* last = reinterpret_cast<uint32_t*>(base + L::OFF_MISC + 8);
         __threadfence();                         // this CTA's partials before its count
         __syncthreads();
@@ -697,28 +797,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
 }
 
-template <int D, int CS>
-cudaError_t launch_tc(const AttnArgs& a, const TcMaps& m, cudaStream_t st) {
+template <int D, int CS, bool SPLIT>
+cudaError_t launch_grid(const AttnArgs& a, const TcMaps& m, cudaStream_t st, int grid) {
     using L = TcLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, CS>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, CS, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    const int n_slots = (a.n_row_tiles + CS - 1) / CS * CS;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.U * n_slots));
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(L::THREADS);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.x = SPLIT ? 2 : CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, CS>, m.k, m.v, a);
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, CS, SPLIT>, m.k, m.v, a);
+}
+
+// Query tiles run as a key-split pair: the tiles of the last, partial wave
+// (one CTA per SM, a.resident SMs), when it fills at most half the SMs after
+// at least one full wave.  STATEKV_ATTN_SPLIT overrides: 0 = none, all =
+// every tile, n = the last n tiles.
+int split_tiles(int items, int resident) {
+    const char* env = std::getenv("STATEKV_ATTN_SPLIT");
+    if (env && *env) {
+        if (std::strcmp(env, "all") == 0) return items;
+        const long n = std::strtol(env, nullptr, 10);
+        return (int)std::max(0L, std::min((long)items, n));
+    }
+    if (resident <= 0) return 0;
+    const int full = items / resident * resident, tail = items - full;
+    return (full > 0 && tail > 0 && 2 * tail <= resident) ? tail : 0;
+}
+
+template <int D, int CS>
+cudaError_t launch_tc(const AttnArgs& a_in, const TcMaps& m, cudaStream_t st) {
+    const int n_slots = (a_in.n_row_tiles + CS - 1) / CS * CS;
+    const int items = a_in.U * n_slots;
+    if (CS > 1) return launch_grid<D, CS, false>(a_in, m, st, items);
+    AttnArgs a = a_in;
+    int split = split_tiles(items, a.resident);
+    if (split == 0) {
+        a.split_item0 = items;
+        return launch_grid<D, 1, false>(a, m, st, items);
+    }
+    // whole tiles go two per cluster: an even count
+    if ((items - split) & 1) ++split;
+    a.split_item0 = items - split;
+    cudaError_t e = launch_grid<D, 1, true>(a, m, st, a.split_item0 + 2 * split);
+    return e;
 }
 
 }  // namespace

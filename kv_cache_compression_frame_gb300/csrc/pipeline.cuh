@@ -36,6 +36,22 @@ struct Sync {
             }
         }
     }
+    // wait() for a barrier that the other CTA of a cluster arrives on after
+    // writing into this CTA's shared memory (acquire at cluster scope)
+    __device__ bool wait_cluster(int i, uint32_t parity, uint32_t site) const {
+        const uint32_t b = bar(i);
+        if (ptx::mbar_poll_cluster(b, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            if (ptx::mbar_wait_hint_cluster(b, parity, 20000u)) return true;
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kTimeoutNs) {
+                *abort = 1u;
+                record_error(err, (uint32_t)STATEKV_E_TIMEOUT, site, (uint32_t)i);
+                return false;
+            }
+        }
+    }
     // Teardown wait: ignores the abort flag, still bounded.
     __device__ void drain(int i, uint32_t parity) const {
         const uint32_t b = bar(i);

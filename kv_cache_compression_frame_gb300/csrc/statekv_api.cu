@@ -229,6 +229,7 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     const bool tc = c.dtype == STATEKV_BF16;
     if (tc) { aa.unit_done = h->unit_done; aa.scores = h->scores; }
     aa.inv_rows = (float)(1.0 / ((double)h->G * T));
+    aa.resident = h->num_sms;                            // one attention CTA per SM
     e = timed(h, STATEKV_KERNEL_ATTENTION, st, [&] {
         return c.dtype == STATEKV_BF16 ? launch_attention_tc(aa, h->tc, st)
                                        : launch_attention_simt(aa, st);

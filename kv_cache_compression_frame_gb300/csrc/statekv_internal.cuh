@@ -67,6 +67,11 @@ struct AttnArgs {
     uint32_t* unit_done;  // [U] counters, zero between launches (or null)
     float* scores;        // [U][m_pad] s_j = sum of the partials / (G*T)
     float inv_rows;       // 1 / (G*T)
+    // query tiles [split_item0, U * n_row_tiles) run as key-split CTA pairs
+    // (set by the launcher); resident = CTAs one wave holds (one per SM; 0:
+    // never split)
+    int32_t split_item0;
+    int32_t resident;
 };
 
 struct SelectArgs {

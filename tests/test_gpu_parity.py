@@ -425,3 +425,20 @@ def test_overlapped_launches_match_serialised():
         for x, y in zip(ca[l], cb[l]):
             assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
                                y.view(torch.int16) if y.dtype == torch.bfloat16 else y), f"C of layer {l}"
+
+
+@pytest.mark.parametrize("split,head_dim,q_heads,kv_heads,T,B", [
+    ("all", 128, 8, 2, 128, 256),     # every query tile as a key-split CTA pair
+    ("all", 64, 6, 2, 3, 7),          # one-tile keys: one half holds none
+    ("3", 128, 6, 2, 64, 200),        # the last three tiles split, the rest whole
+])
+def test_key_split_query_tiles(split, head_dim, q_heads, kv_heads, T, B, monkeypatch):
+    """Query tiles computed by two CTAs of a cluster, one key half each
+    (lse partials and O columns exchanged through distributed shared
+    memory): every frame against the oracle."""
+    monkeypatch.setenv("STATEKV_ATTN_SPLIT", split)
+    sh = _small("split", q_heads=q_heads, kv_heads=kv_heads, head_dim=head_dim,
+                frame_tokens=T, budget=B, frames=6)
+    st = Stepper(sh)
+    for n in range(sh.frames):
+        st.step(n)
