@@ -114,6 +114,13 @@ typedef struct statekv_handle statekv_handle;   /* opaque */
  * multicast within a thread-block cluster of that size (fewer L2 reads,
  * coupled pipelines; results are bit-identical).  Unset or any other value:
  * one CTA per query tile, the measured-faster default.
+ * With one CTA per query tile, the tiles of the last, partial wave (when it
+ * fills at most half the SMs after at least one full wave) are each
+ * computed by two CTAs of a cluster, one half of the key tiles each, which
+ * exchange their row log-sum-exps and output halves through distributed
+ * shared memory; results agree with whole tiles up to rounding.
+ * STATEKV_ATTN_SPLIT, read at every prefill launch, overrides which tiles
+ * do so: 0 = none, all = every tile, n = the last n tiles.
  */
 typedef struct statekv_config {
     int32_t num_streams;
