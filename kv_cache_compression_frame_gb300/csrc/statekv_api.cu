@@ -13,6 +13,7 @@
 //   Q'         [U*G*T][d]       rotated queries (scratch)
 //   colsum     [U][tiles][m_pad] per query-tile column sums of P
 //   scores     [U][m_pad], score_pos [U][m_pad]
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -72,8 +73,10 @@ struct statekv_handle {
     // entry point (streams and events are created on its first call)
     void* stage2_q = nullptr; void* stage2_k = nullptr; void* stage2_v = nullptr;
     void* stage2_o = nullptr;
-    cudaStream_t s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev_entry = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+    // two copy streams per direction: one copy stream moved ~100 GB/s, less
+    // than a frame's 29 MB in per frame time needs
+    cudaStream_t s_in[2] = {}, s_out[2] = {};
+    cudaEvent_t ev_entry = nullptr, ev_in[2][2] = {}, ev_front[2] = {}, ev_out[2][2] = {};
     TcMaps tc{};                        // TMA views for the bf16 attention kernel
 
     bool profiling = false;
@@ -97,6 +100,15 @@ struct statekv_handle {
 
 namespace {
 
+void destroy_pipeline(statekv_handle* h) {
+    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0][0], &h->ev_in[0][1], &h->ev_in[1][0],
+                           &h->ev_in[1][1], &h->ev_front[0], &h->ev_front[1], &h->ev_out[0][0],
+                           &h->ev_out[0][1], &h->ev_out[1][0], &h->ev_out[1][1]})
+        if (*e) { cudaEventDestroy(*e); *e = nullptr; }
+    for (cudaStream_t* st : {&h->s_in[0], &h->s_in[1], &h->s_out[0], &h->s_out[1]})
+        if (*st) { cudaStreamDestroy(*st); *st = nullptr; }
+}
+
 void free_all(statekv_handle* h) {
     for (void* p : h->allocs) cudaFree(p);
     h->allocs.clear();
@@ -104,11 +116,7 @@ void free_all(statekv_handle* h) {
     for (auto e : h->spare) cudaEventDestroy(e);
     h->pending.clear();
     h->spare.clear();
-    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0], &h->ev_comp[1],
-                           &h->ev_out[0], &h->ev_out[1]})
-        if (*e) { cudaEventDestroy(*e); *e = nullptr; }
-    for (cudaStream_t* st : {&h->s_in, &h->s_out})
-        if (*st) { cudaStreamDestroy(*st); *st = nullptr; }
+    destroy_pipeline(h);
 }
 
 template <typename T>
@@ -200,7 +208,11 @@ int check_ptr(const void* p) {
     return STATEKV_OK;
 }
 
-int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, void* o,
+// One frame step in two halves: RoPE + attention (reads q, k, v, writes o),
+// then the selection.  A caller may put waits between the halves: there they
+// cost nothing, while between the selection and the next frame's RoPE they
+// would end the overlap of the two (programmatic dependent launch).
+int run_front(statekv_handle* h, const void* q, const void* k, const void* v, void* o,
               cudaStream_t st) {
     const statekv_config& c = h->cfg;
     const int T = c.frame_tokens, d = c.head_dim;
@@ -235,7 +247,15 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
                                        : launch_attention_simt(aa, st);
     });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
+    return STATEKV_OK;
+}
 
+int run_back(statekv_handle* h, cudaStream_t st) {
+    const statekv_config& c = h->cfg;
+    const int T = c.frame_tokens, d = c.head_dim;
+    const int cc = h->c();
+    const int64_t p0 = c.position_offset + h->n * T;
+    const bool tc = c.dtype == STATEKV_BF16;
     SelectArgs sa{};
     sa.colsum = h->colsum; sa.scores = h->scores; sa.score_pos = h->score_pos;
     sa.pos = h->pos; sa.pool_k = h->pool_k; sa.pool_v = h->pool_v; sa.err = h->err;
@@ -246,11 +266,17 @@ int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, vo
     sa.window = c.select_policy == STATEKV_SELECT_WINDOW;
     sa.scores_done = tc;
     sa.never_evicts = (int64_t)c.budget >= (int64_t)c.max_frames * T;
-    e = timed(h, STATEKV_KERNEL_SELECT, st, [&] { return launch_select(sa, st); });
+    cudaError_t e = timed(h, STATEKV_KERNEL_SELECT, st, [&] { return launch_select(sa, st); });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
 
     h->n += 1;
     return STATEKV_OK;
+}
+
+int run_frame(statekv_handle* h, const void* q, const void* k, const void* v, void* o,
+              cudaStream_t st) {
+    const int r = run_front(h, q, k, v, o, st);
+    return r != STATEKV_OK ? r : run_back(h, st);
 }
 
 }  // namespace
@@ -394,18 +420,16 @@ int statekv_prefill_frame_host(statekv_handle* h, const void* q, const void* k, 
 namespace {
 
 bool ensure_pipeline(statekv_handle* h) {
-    if (h->s_in) return true;
-    bool ok = cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess;
-    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0],
-                           &h->ev_comp[1], &h->ev_out[0], &h->ev_out[1]})
+    if (h->s_in[0]) return true;
+    bool ok = true;
+    for (cudaStream_t* st : {&h->s_in[0], &h->s_in[1], &h->s_out[0], &h->s_out[1]})
+        ok = ok && cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0][0], &h->ev_in[0][1], &h->ev_in[1][0],
+                           &h->ev_in[1][1], &h->ev_front[0], &h->ev_front[1], &h->ev_out[0][0],
+                           &h->ev_out[0][1], &h->ev_out[1][0], &h->ev_out[1][1]})
         ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
-        for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0],
-                               &h->ev_comp[1], &h->ev_out[0], &h->ev_out[1]})
-            if (*e) { cudaEventDestroy(*e); *e = nullptr; }
-        for (cudaStream_t* st : {&h->s_in, &h->s_out})
-            if (*st) { cudaStreamDestroy(*st); *st = nullptr; }
+        destroy_pipeline(h);
         cudaGetLastError();
     }
     return ok;
@@ -413,13 +437,18 @@ bool ensure_pipeline(statekv_handle* h) {
 
 }  // namespace
 
-// Frames i = 0..F-1, staging slot i & 1:
-//   s_in : [wait compute(i-2)] H2D q,k,v(i) -> slot          record ev_in[slot]
-//   st   : wait ev_in[slot], [wait D2H(i-2)] step(i)          record ev_comp[slot]
-//   s_out: wait ev_comp[slot]  D2H o(i) <- slot                record ev_out[slot]
-// so the copies of frames i+1 (in) and i-1 (out) overlap the step of frame i.
-// Both side streams first wait for everything already on st; at the end st
-// waits for the last D2H, so the batch is ordered on st like one call.
+// Frames i = 0..F-1, staging slot i & 1; each copy is split over two streams
+// (j = 0, 1) of each direction:
+//   s_in[j] : [wait front(i-2)] H2D part j of q,k,v(i) -> slot     record ev_in[slot][j]
+//   st      : front(i) (RoPE, attention)                         record ev_front[slot]
+//   s_out[j]: wait ev_front[slot]  D2H part j of o(i) <- slot       record ev_out[slot][j]
+//   st      : wait ev_in[next slot], [wait ev_out[next slot] of frame i-1],
+//             back(i) (selection)
+// so the copies of frames i+1 (in) and i (out) overlap the step of frame
+// i, and the waits sit between the attention and the selection, never
+// between the selection and the next frame's RoPE.  The side streams first
+// wait for everything already on st; at the end st waits for the last
+// copies, so the batch is ordered on st like one call.
 int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q, const void* k,
                                 const void* v, void* o, void* cuda_stream) {
     if (!h || frames < 0 || !q || !k || !v || !o || h->text > 0) return STATEKV_E_INVALID_ARG;
@@ -434,33 +463,63 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
     void* sk[2] = {h->stage_k, h->stage2_k};
     void* sv[2] = {h->stage_v, h->stage2_v};
     void* so[2] = {h->stage_o, h->stage2_o};
+    // input part 0: the first qa bytes of q; part 1: the rest of q, k and v
+    const size_t qa = std::min(qb, ((qb + 2 * kvb) / 2 + 255) / 256 * 256);
+    const size_t oa = (qb / 2 + 255) / 256 * 256;      // output part 0: o[0, oa)
     auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-    if (!ok(cudaEventRecord(h->ev_entry, st)) || !ok(cudaStreamWaitEvent(h->s_in, h->ev_entry, 0)) ||
-        !ok(cudaStreamWaitEvent(h->s_out, h->ev_entry, 0)))
-        return STATEKV_E_CUDA;
-    for (int32_t i = 0; i < frames; ++i) {
+    if (!ok(cudaEventRecord(h->ev_entry, st))) return STATEKV_E_CUDA;
+    for (int j = 0; j < 2; ++j)
+        if (!ok(cudaStreamWaitEvent(h->s_in[j], h->ev_entry, 0)) ||
+            !ok(cudaStreamWaitEvent(h->s_out[j], h->ev_entry, 0)))
+            return STATEKV_E_CUDA;
+    auto h2d = [&](int32_t i) -> bool {
         const int sl = i & 1;
         const char* qi = static_cast<const char*>(q) + (size_t)i * qb;
         const char* ki = static_cast<const char*>(k) + (size_t)i * kvb;
         const char* vi = static_cast<const char*>(v) + (size_t)i * kvb;
-        char* oi = static_cast<char*>(o) + (size_t)i * qb;
-        if (i >= 2 && !ok(cudaStreamWaitEvent(h->s_in, h->ev_comp[sl], 0))) return STATEKV_E_CUDA;
-        if (!ok(cudaMemcpyAsync(sq[sl], qi, qb, cudaMemcpyHostToDevice, h->s_in)) ||
-            !ok(cudaMemcpyAsync(sk[sl], ki, kvb, cudaMemcpyHostToDevice, h->s_in)) ||
-            !ok(cudaMemcpyAsync(sv[sl], vi, kvb, cudaMemcpyHostToDevice, h->s_in)) ||
-            !ok(cudaEventRecord(h->ev_in[sl], h->s_in)) ||
-            !ok(cudaStreamWaitEvent(st, h->ev_in[sl], 0)))
-            return STATEKV_E_CUDA;
-        if (i >= 2 && !ok(cudaStreamWaitEvent(st, h->ev_out[sl], 0))) return STATEKV_E_CUDA;
-        const int r = run_frame(h, sq[sl], sk[sl], sv[sl], so[sl], st);
+        char* dq = static_cast<char*>(sq[sl]);
+        for (int j = 0; j < 2; ++j)
+            if (i >= 2 && !ok(cudaStreamWaitEvent(h->s_in[j], h->ev_front[sl], 0))) return false;
+        return ok(cudaMemcpyAsync(dq, qi, qa, cudaMemcpyHostToDevice, h->s_in[0])) &&
+               ok(cudaEventRecord(h->ev_in[sl][0], h->s_in[0])) &&
+               (qa == qb || ok(cudaMemcpyAsync(dq + qa, qi + qa, qb - qa, cudaMemcpyHostToDevice,
+                                               h->s_in[1]))) &&
+               ok(cudaMemcpyAsync(sk[sl], ki, kvb, cudaMemcpyHostToDevice, h->s_in[1])) &&
+               ok(cudaMemcpyAsync(sv[sl], vi, kvb, cudaMemcpyHostToDevice, h->s_in[1])) &&
+               ok(cudaEventRecord(h->ev_in[sl][1], h->s_in[1])) &&
+               ok(cudaStreamWaitEvent(st, h->ev_in[sl][0], 0)) &&
+               ok(cudaStreamWaitEvent(st, h->ev_in[sl][1], 0));
+    };
+    if (!h2d(0)) return STATEKV_E_CUDA;
+    for (int32_t i = 0; i < frames; ++i) {
+        const int sl = i & 1;
+        int r = run_front(h, sq[sl], sk[sl], sv[sl], so[sl], st);
         if (r != STATEKV_OK) return r;
-        if (!ok(cudaEventRecord(h->ev_comp[sl], st)) ||
-            !ok(cudaStreamWaitEvent(h->s_out, h->ev_comp[sl], 0)) ||
-            !ok(cudaMemcpyAsync(oi, so[sl], qb, cudaMemcpyDeviceToHost, h->s_out)) ||
-            !ok(cudaEventRecord(h->ev_out[sl], h->s_out)))
-            return STATEKV_E_CUDA;
+        if (!ok(cudaEventRecord(h->ev_front[sl], st))) return STATEKV_E_CUDA;
+        char* oi = static_cast<char*>(o) + (size_t)i * qb;
+        const char* ds = static_cast<const char*>(so[sl]);
+        for (int j = 0; j < 2; ++j) {
+            const size_t b0 = j ? oa : 0, b1 = j ? qb : oa;
+            if (!ok(cudaStreamWaitEvent(h->s_out[j], h->ev_front[sl], 0)) ||
+                (b1 > b0 && !ok(cudaMemcpyAsync(oi + b0, ds + b0, b1 - b0, cudaMemcpyDeviceToHost,
+                                                h->s_out[j]))) ||
+                !ok(cudaEventRecord(h->ev_out[sl][j], h->s_out[j])))
+                return STATEKV_E_CUDA;
+        }
+        if (i + 1 < frames) {
+            if (!h2d(i + 1)) return STATEKV_E_CUDA;
+            // attention(i+1) rewrites the output slot of frame i-1
+            for (int j = 0; j < 2; ++j)
+                if (i >= 1 && !ok(cudaStreamWaitEvent(st, h->ev_out[(i + 1) & 1][j], 0)))
+                    return STATEKV_E_CUDA;
+        }
+        r = run_back(h, st);
+        if (r != STATEKV_OK) return r;
     }
-    if (!ok(cudaStreamWaitEvent(st, h->ev_out[(frames - 1) & 1], 0))) return STATEKV_E_CUDA;
+    for (int s2 = 0; s2 < 2 && s2 < frames; ++s2)
+        for (int j = 0; j < 2; ++j)
+            if (!ok(cudaStreamWaitEvent(st, h->ev_out[(frames - 1 - s2) & 1][j], 0)))
+                return STATEKV_E_CUDA;
     return STATEKV_OK;
 }
 
