@@ -6,7 +6,8 @@
 //     compressed key is visible, frame keys are causal;
 //   关键设计 2 -- key j's importance is the attention the frame's queries pay
 //     to it, averaged over queries; this kernel emits, per 128-row query
-//     tile, the column sums of the final normalised P;
+//     tile, the column sums of the final normalised P (the select kernel
+//     adds the tiles' partials in tile order);
 //   整体框架 -- the per-frame cost O(T^2 + BT): the key loop covers only the
 //     B compressed keys and the causally visible part of the frame.
 //
@@ -760,8 +761,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::tc_fence_before();
     }
 
-    // a split pair counts once, by half 0, after half 1's partials are out
-    if (coop) __threadfence();
     __syncthreads();
     // no CTA leaves while a peer may still multicast into it or arrive on
     // its barriers (every role above has drained its own traffic)
@@ -769,31 +768,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, L::TMEM_COLS);
-    }
-    // ---- scores (关键设计 2): the last of the unit's query-tile CTAs to
-    // finish sums every tile's column partials in tile order (the fixed
-    // order keeps s_j bit-reproducible) while other units still run
-    if (a.unit_done != nullptr && mt < n_rt && (!coop || half == 0)) {
-        uint32_t* last = reinterpret_cast<uint32_t*>(base + L::OFF_MISC + 8);
-        __threadfence();                         // this CTA's partials before its count
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t prev = atomicAdd(&a.unit_done[u], 1u);
-            *last = prev == (uint32_t)(n_rt - 1) ? 1u : 0u;
-        }
-        __syncthreads();
-        if (*last) {
-            __threadfence();
-            const int m = a.c + a.T;
-            const float* cs = a.colsum + (int64_t)u * n_rt * a.m_pad;
-            float* sc = a.scores + (int64_t)u * a.m_pad;
-            for (int j = threadIdx.x; j < m; j += blockDim.x) {
-                float acc = 0.f;
-                for (int t = 0; t < n_rt; ++t) acc += __ldcg(cs + (int64_t)t * a.m_pad + j);
-                sc[j] = acc * a.inv_rows;
-            }
-            if (threadIdx.x == 0) a.unit_done[u] = 0u;   // ready for the next launch
-        }
     }
 }
 

@@ -7,8 +7,7 @@
 //
 // One CTA per (stream, layer, KV head):
 //   1. s_j = (sum over query-row tiles of the column sums of P) / (G*T), in a
-//      fixed tile order (deterministic) -- unless the attention kernel's last
-//      CTA of the unit already did it (same order, same bits);
+//      fixed tile order (deterministic);
 //   2. every candidate gets the 64-bit key (float bits of s_j) << 32 |
 //      ~position: s_j >= 0, so the bit pattern orders like the value, and the
 //      complemented position makes the lower position win a tie.  Keys are
@@ -61,13 +60,16 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     const int m = c + T;
     int32_t* pos = a.pos + (int64_t)u * a.slots;
 
-    // ---- 1-2. scores, positions, keys (each thread's loads issued before
-    // its stores: the position and score buffers may alias as far as the
-    // compiler knows, which would otherwise serialise one round trip per key)
+    // ---- 1-2. scores, positions, keys.  A thread issues every load of its
+    // KU keys (the partials of up to TU query tiles each, and the positions)
+    // before it adds or stores anything: one memory round trip per KU keys
+    // instead of one per tile (the position and score buffers may alias as
+    // far as the compiler knows, which would otherwise serialise them too)
     const float* cs = a.colsum + (int64_t)u * a.n_row_tiles * a.m_pad;
     float* scores = a.scores + (int64_t)u * a.m_pad;
     int32_t* spos = a.score_pos + (int64_t)u * a.m_pad;
-    constexpr int KU = 4;
+    constexpr int KU = 2, TU = 12;
+    const int n_rt = a.n_row_tiles;
     uint64_t k_and = ~0ull, k_or = 0ull;
     for (int j0 = tid; j0 < m; j0 += KU * kThreads) {
         float sv[KU];
@@ -77,22 +79,31 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
             const int j = j0 + q * kThreads;
             sv[q] = 0.f;
             pv[q] = 0;
-            if (j < m) {
-                if (a.scores_done) {
-                    sv[q] = scores[j];
-                } else {
-                    float acc = 0.f;
-                    for (int t = 0; t < a.n_row_tiles; ++t) acc += cs[(int64_t)t * a.m_pad + j];
-                    sv[q] = acc * a.inv_rows;
-                }
-                pv[q] = j < c ? pos[j] : a.pos_base + (j - c);
+            if (j < m) pv[q] = j < c ? pos[j] : a.pos_base + (j - c);
+        }
+        for (int t0 = 0; t0 < n_rt; t0 += TU) {
+            float part[KU][TU];
+#pragma unroll
+            for (int q = 0; q < KU; ++q) {
+                const int j = j0 + q * kThreads;
+#pragma unroll
+                for (int tt = 0; tt < TU; ++tt)
+                    part[q][tt] = (j < m && t0 + tt < n_rt)
+                                      ? __ldcg(cs + (int64_t)(t0 + tt) * a.m_pad + j) : 0.f;
             }
+            // tile order: s_j has the same bits whatever the tiling above
+#pragma unroll
+            for (int q = 0; q < KU; ++q)
+#pragma unroll
+                for (int tt = 0; tt < TU; ++tt)
+                    if (t0 + tt < n_rt) sv[q] += part[q][tt];
         }
 #pragma unroll
         for (int q = 0; q < KU; ++q) {
             const int j = j0 + q * kThreads;
             if (j < m) {
-                if (!a.scores_done) scores[j] = sv[q];
+                sv[q] *= a.inv_rows;
+                scores[j] = sv[q];
                 spos[j] = pv[q];
                 if (m > B) {
                     const uint64_t k = a.window ? (uint64_t)(uint32_t)pv[q] << 32 : cand_key(sv[q], pv[q]);

@@ -65,7 +65,6 @@ struct statekv_handle {
     void* q_rot = nullptr;
     float* colsum = nullptr;
     float* scores = nullptr;
-    uint32_t* unit_done = nullptr;      // [U] per-unit CTA counters of the attention kernel
     int32_t* score_pos = nullptr;
     uint32_t* err = nullptr;            // device status word
     void* stage_q = nullptr; void* stage_k = nullptr; void* stage_v = nullptr; void* stage_o = nullptr;
@@ -238,9 +237,6 @@ int run_front(statekv_handle* h, const void* q, const void* k, const void* v, vo
     aa.U = h->U; aa.GT = h->GT; aa.T = T; aa.d = d; aa.slots = h->slots; aa.c = cc;
     aa.m_pad = h->m_pad; aa.n_row_tiles = h->n_row_tiles;
     aa.scale = h->scale; aa.scale_log2 = h->scale_log2;
-    const bool tc = c.dtype == STATEKV_BF16;
-    if (tc) { aa.unit_done = h->unit_done; aa.scores = h->scores; }
-    aa.inv_rows = (float)(1.0 / ((double)h->G * T));
     aa.resident = h->num_sms;                            // one attention CTA per SM
     e = timed(h, STATEKV_KERNEL_ATTENTION, st, [&] {
         return c.dtype == STATEKV_BF16 ? launch_attention_tc(aa, h->tc, st)
@@ -255,7 +251,6 @@ int run_back(statekv_handle* h, cudaStream_t st) {
     const int T = c.frame_tokens, d = c.head_dim;
     const int cc = h->c();
     const int64_t p0 = c.position_offset + h->n * T;
-    const bool tc = c.dtype == STATEKV_BF16;
     SelectArgs sa{};
     sa.colsum = h->colsum; sa.scores = h->scores; sa.score_pos = h->score_pos;
     sa.pos = h->pos; sa.pool_k = h->pool_k; sa.pool_v = h->pool_v; sa.err = h->err;
@@ -264,7 +259,6 @@ int run_back(statekv_handle* h, cudaStream_t st) {
     sa.pos_base = (int32_t)p0;
     sa.inv_rows = (float)(1.0 / ((double)h->G * T));
     sa.window = c.select_policy == STATEKV_SELECT_WINDOW;
-    sa.scores_done = tc;
     sa.never_evicts = (int64_t)c.budget >= (int64_t)c.max_frames * T;
     cudaError_t e = timed(h, STATEKV_KERNEL_SELECT, st, [&] { return launch_select(sa, st); });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
@@ -341,7 +335,6 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     ok = ok && dalloc(h, &h->q_rot, (size_t)h->U * h->GT * row);
     ok = ok && dalloc(h, &h->colsum, sizeof(float) * (size_t)h->U * h->n_row_tiles * h->m_pad);
     ok = ok && dalloc(h, &h->scores, sizeof(float) * (size_t)h->U * h->m_pad);
-    ok = ok && dalloc(h, &h->unit_done, sizeof(uint32_t) * (size_t)h->U);
     ok = ok && dalloc(h, &h->score_pos, sizeof(int32_t) * (size_t)h->U * h->m_pad);
     ok = ok && dalloc(h, &h->err, sizeof(uint32_t) * kErrWords);
     ok = ok && dalloc(h, &h->stage_q, h->q_bytes());

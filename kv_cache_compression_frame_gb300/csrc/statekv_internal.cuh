@@ -63,10 +63,6 @@ struct AttnArgs {
     int32_t U, GT, T, d, slots, c, m_pad, n_row_tiles;
     float scale_log2;     // mscale^2/sqrt(d) * log2(e)
     float scale;          // mscale^2/sqrt(d)
-    // optional: the last CTA of each unit turns the partials into the scores
-    uint32_t* unit_done;  // [U] counters, zero between launches (or null)
-    float* scores;        // [U][m_pad] s_j = sum of the partials / (G*T)
-    float inv_rows;       // 1 / (G*T)
     // query tiles [split_item0, U * n_row_tiles) run as key-split CTA pairs
     // (set by the launcher); resident = CTAs one wave holds (one per SM; 0:
     // never split)
@@ -85,7 +81,6 @@ struct SelectArgs {
     int32_t pos_base;     // virtual position of this frame's token 0
     float inv_rows;       // 1 / (G*T)
     int32_t window;       // 1: keep the B most recent tokens instead of Top-B
-    int32_t scores_done;  // 1: scores already summed (by the attention kernel)
     int32_t never_evicts; // B >= every pool size this handle can reach
 };
 
