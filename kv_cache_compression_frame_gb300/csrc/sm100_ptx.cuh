@@ -372,27 +372,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
         : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
-// 2^x for a pair of x <= 0 on the FMA/ALU pipes instead of the MUFU unit
-// (Cody-Waite style split): x is clamped at -125, n = round(x) is produced by
-// adding 1.5*2^23 (its integer lands in the low mantissa bits), f = x - n in
-// [-0.5, 0.5], 2^f comes from a degree-4 polynomial least-squares fitted to
-// 2^f at Chebyshev nodes on [-0.5, 0.5] (max relative error 2.7e-6 in fp32
-// Horner form), and n is added to the result's exponent field.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    const float2 magic = make_float2(12582912.0f, 12582912.0f);
-    x.x = fmaxf(x.x, -125.0f);
-    x.y = fmaxf(x.y, -125.0f);
-    const float2 r = add2(x, magic);
-    const float2 n = add2(r, make_float2(-12582912.0f, -12582912.0f));
-    const float2 f = fma2(n, make_float2(-1.0f, -1.0f), x);
-    float2 p = fma2(make_float2(0.009560510516166687f, 0.009560510516166687f), f,
-                    make_float2(0.05591703951358795f, 0.05591703951358795f));
-    p = fma2(p, f, make_float2(0.24024981260299683f, 0.24024981260299683f));
-    p = fma2(p, f, make_float2(0.6931219696998596f, 0.6931219696998596f));
-    p = fma2(p, f, make_float2(0.9999991655349731f, 0.9999991655349731f));
-    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(r.x) << 23)),
-                       __int_as_float(__float_as_int(p.y) + (__float_as_int(r.y) << 23)));
-}
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
