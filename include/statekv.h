@@ -312,8 +312,10 @@ int statekv_set_compressed(statekv_handle* h, int32_t s, int32_t layer,
  * Overlap of consecutive launches within a frame sequence: the RoPE kernel
  * of frame n+1 starts while the selection of frame n still runs (its query
  * rows do not depend on it; its writes of the frame's keys into the pool
- * wait for the selection to finish), and the attention kernel's set-up
- * overlaps the RoPE kernel's end (programmatic dependent launch).  Any other
+ * wait for the selection to finish), the attention kernel's set-up
+ * overlaps the RoPE kernel's end, and the selection is launched while the
+ * attention kernel still runs and starts work as soon as it has finished
+ * (programmatic dependent launch).  Any other
  * operation on the stream between two calls separates them as usual.
  */
 int statekv_profile_enable(statekv_handle* h, int enable);

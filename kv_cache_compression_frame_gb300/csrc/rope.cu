@@ -145,10 +145,10 @@ cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st) {
 }
 
 // early: the kernel may start while the previous kernel of the stream (the
-// previous frame's selection, which triggers its dependents at its start)
-// still runs.  Safe because that selection started only after the previous
-// frame's attention ended, so Q' (read by that attention) may be rewritten
-// at once, and the pool rows the selection reads are written after
+// previous frame's selection, which triggers its dependents as soon as it
+// has waited for the attention kernel before it) still runs.  Safe because
+// that attention has then ended, so Q' (read by it) may be rewritten at
+// once, and the pool rows the selection reads are written after
 // dep_wait().  Inputs q, k, v were written before the selection was queued
 // or by an operation between the two, which then orders them as usual.
 cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st, bool early) {

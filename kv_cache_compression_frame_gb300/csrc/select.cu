@@ -50,8 +50,12 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     __shared__ uint32_t s_rank;
     __shared__ uint32_t s_unique;
 
-    // the next frame's RoPE kernel may start now (it waits for this grid
-    // before it writes the pool rows read here)
+    // launched while the attention kernel still runs (programmatic dependent
+    // launch): its column partials and the pool are read only after it has
+    // finished.  Then the next frame's RoPE kernel may start (it rewrites
+    // Q', which the attention kernel read, and waits for this grid before
+    // it writes the pool rows read here)
+    ptx::dep_wait();
     ptx::dep_trigger();
     const int u = blockIdx.x;
     const int tid = threadIdx.x;
@@ -323,8 +327,17 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel,
         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    select_kernel<<<a.U, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.U);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, select_kernel, a);
 }
 
 }  // namespace statekv

@@ -209,8 +209,10 @@ int check_ptr(const void* p) {
 
 // One frame step in two halves: RoPE + attention (reads q, k, v, writes o),
 // then the selection.  A caller may put waits between the halves: there they
-// cost nothing, while between the selection and the next frame's RoPE they
-// would end the overlap of the two (programmatic dependent launch).
+// cost only the selection's early launch (its CTAs then start when the wait
+// is over instead of waiting on the GPU for the attention kernel), while
+// between the selection and the next frame's RoPE they would end the overlap
+// of the two (programmatic dependent launch).
 int run_front(statekv_handle* h, const void* q, const void* k, const void* v, void* o,
               cudaStream_t st) {
     const statekv_config& c = h->cfg;
