@@ -347,6 +347,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         uint32_t pv_par = 0;                           // parity of the next P_FULL phase
         const float* colbuf = reinterpret_cast<const float*>(base + L::OFF_COL);
         float* colsum = a.colsum + ((int64_t)u * n_rt + mt) * a.m_pad;
+        const uint64_t keep_l2 = ptx::l2_policy_evict_last();
         // sweep 1: the odd S tiles (warp 1 issues the even ones)
         bool ok = sy.wait(L::B_Q, 0, kSiteQFull);
         ptx::tc_fence_after();
@@ -388,12 +389,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             __syncwarp();
             if (mine) {
                 pv_par ^= 1u;
-                // key column sums of P(t): the 4 lane quarters' partials
+                // key column sums of P(t): the 4 lane quarters' partials (kept
+                // in L2 for the select kernel that reads them after this grid)
                 const float* cb = colbuf + (t % L::NCOL) * 512;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int e = 32 * j + lane;
-                    colsum[(t0 + t) * L::BN + e] = cb[e] + cb[128 + e] + cb[256 + e] + cb[384 + e];
+                    ptx::st_global_hint(colsum + (t0 + t) * L::BN + e,
+                                        cb[e] + cb[128 + e] + cb[256 + e] + cb[384 + e], keep_l2);
                 }
             }
         }
