@@ -8,21 +8,24 @@
 // One CTA per (stream, layer, KV head):
 //   1. s_j = (sum over query-row tiles of the column sums of P) / (G*T), in a
 //      fixed tile order (deterministic);
-//   2. every candidate gets the 64-bit key (float bits of s_j) << 32 |
-//      ~position: s_j >= 0, so the bit pattern orders like the value, and the
-//      complemented position makes the lower position win a tie.  Keys are
-//      distinct, so "keep the B largest keys" is exactly Top-B with the tie
-//      rule;
-//   3. an MSB-first radix select (8-bit digits from the highest bit where
-//      keys differ; histograms shared by warp pairs) finds the E-th smallest
-//      key, E = m - B;
-//      keys at or below it are evicted;
+//   2. every candidate gets the 32-bit key "float bits of s_j": s_j >= 0, so
+//      the bit pattern orders like the value;
+//   3. an MSB-first radix select (11-bit digits from the highest bit where
+//      keys differ) finds where the E = m - B smallest keys end; it stops as
+//      soon as the boundary bucket is evicted whole.  Only if that leaves
+//      keys of exactly equal score on both sides of the cut does a second
+//      radix select over their positions pick the lower positions to keep
+//      (the tie rule);
 //      (window policy, the sliding-window baseline: the key is the position,
 //      so the B most recent tokens are kept);
 //   4. slot reuse: the pool is [compressed slots 0..c) ; frame rows c..c+T).
 //      Evicted slots below B ("holes") are refilled by surviving rows at or
 //      above B ("movers"), paired in slot order; only those rows move
 //      (<= T rows of K and V per unit instead of rewriting all B).
+// Every step is written for 32 warps that share each sub-partition eight
+// ways: per-thread work is kept to a few instructions per key (32-bit keys,
+// warp ballots for the slot-ordered lists), since each one costs eight
+// issue slots.
 #include "statekv_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -30,25 +33,125 @@ namespace statekv {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kHists = 16;                      // radix histograms, each shared by 2 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kDigit = 11;                      // radix digit width
+constexpr int kBuckets = 1 << kDigit;
+constexpr int kCopies = 4;                      // histogram copies: warp w counts into w % kCopies
 
-__device__ __forceinline__ uint64_t cand_key(float s, int32_t pos) {
-    return ((uint64_t)__float_as_uint(s) << 32) | (uint64_t)(0xffffffffu - (uint32_t)pos);
+// Where the R smallest of a set of 32-bit keys end: keys k with
+// (k >> shift) < pre are among them, the cnt keys with (k >> shift) == pre
+// are at the boundary (the r smallest of them are among them; all if
+// r == cnt), larger keys are not.  shift = 32 compares nothing.
+struct Cut {
+    uint32_t shift, pre, r, cnt;
+};
+__device__ __forceinline__ uint32_t hi_bits(uint32_t k, uint32_t shift) {
+    return (uint32_t)((uint64_t)k >> shift);
+}
+
+struct RadixScratch {
+    uint32_t* hist;                             // [kCopies][kBuckets], zero on entry and exit
+    uint32_t* comb;                             // [kBuckets] the copies' sum
+    uint32_t* gtot;                             // [kWarps] per 64-bucket group
+    uint32_t* out;                              // [3] bucket, rank in it, its count
+};
+
+// The cut of the R smallest among the n active keys (1 <= R <= n; key_of(j,
+// k) says whether candidate j is active and sets its key); k_and / k_or are
+// the AND and OR of the active keys: their common high bits need no pass.
+template <class KeyOf>
+__device__ Cut radix_cut(const KeyOf& key_of, int m, uint32_t n, uint32_t R, uint32_t k_and,
+                         uint32_t k_or, const RadixScratch& rs) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t diff = k_and ^ k_or;
+    Cut q;
+    q.shift = diff ? 32u - (uint32_t)__clz(diff) : 0u;
+    q.pre = hi_bits(k_and, q.shift);
+    q.r = R;
+    q.cnt = n;
+    while (q.shift > 0 && q.r != q.cnt) {
+        const uint32_t w = min((uint32_t)kDigit, q.shift), sh = q.shift - w;
+        const uint32_t dmask = (1u << w) - 1u;
+        uint32_t* h = rs.hist + (warp % kCopies) * kBuckets;
+        for (int j = tid; j < m; j += kThreads) {
+            uint32_t k;
+            if (key_of(j, k) && hi_bits(k, q.shift) == q.pre) atomicAdd(&h[(k >> sh) & dmask], 1u);
+        }
+        __syncthreads();
+        {   // bucket totals; warp g also sums group g (buckets 64g .. 64g+63)
+            const int b0 = warp * 64 + lane, b1 = b0 + 32;
+            uint32_t c0 = 0, c1 = 0;
+#pragma unroll
+            for (int cp = 0; cp < kCopies; ++cp) {
+                c0 += rs.hist[cp * kBuckets + b0];
+                c1 += rs.hist[cp * kBuckets + b1];
+            }
+            rs.comb[b0] = c0;
+            rs.comb[b1] = c1;
+            const uint32_t g = __reduce_add_sync(0xffffffffu, c0 + c1);
+            if (lane == 0) rs.gtot[warp] = g;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // the group holding the r-th key, then its bucket (two per lane)
+            const uint32_t g = rs.gtot[lane];
+            uint32_t incl = g;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const uint32_t excl = incl - g;
+            const int gs = __ffs(__ballot_sync(0xffffffffu, excl < q.r && q.r <= incl)) - 1;
+            const uint32_t base = __shfl_sync(0xffffffffu, excl, gs);
+            const uint32_t x0 = rs.comb[gs * 64 + 2 * lane], x1 = rs.comb[gs * 64 + 2 * lane + 1];
+            uint32_t inc2 = x0 + x1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, inc2, off);
+                if (lane >= off) inc2 += y;
+            }
+            const uint32_t e0 = base + inc2 - x0 - x1;          // keys below bucket 2*lane
+            if (e0 < q.r && q.r <= e0 + x0) {
+                rs.out[0] = (uint32_t)(gs * 64 + 2 * lane);
+                rs.out[1] = q.r - e0;
+                rs.out[2] = x0;
+            } else if (e0 + x0 < q.r && q.r <= e0 + x0 + x1) {
+                rs.out[0] = (uint32_t)(gs * 64 + 2 * lane + 1);
+                rs.out[1] = q.r - e0 - x0;
+                rs.out[2] = x1;
+            }
+        } else {
+            // the copies are summed into comb: clear them for the next digit
+            uint4* hv = reinterpret_cast<uint4*>(rs.hist);
+            for (int e = tid - 32; e < kCopies * kBuckets / 4; e += kThreads - 32)
+                hv[e] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncthreads();
+        q.pre = (q.pre << w) | rs.out[0];
+        q.r = rs.out[1];
+        q.cnt = rs.out[2];
+        q.shift = sh;
+    }
+    return q;
 }
 
 __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);          // [slots]
-    uint32_t* whist = reinterpret_cast<uint32_t*>(keys + a.slots);   // [kHists][256]
-    uint32_t* kept_bits = whist + kHists * 256;                      // [ceil(slots/32)]
-    // holes / movers [T] each reuse the key buffer once the keys are dead
-    int32_t* holes = reinterpret_cast<int32_t*>(keys);
-    int32_t* movers = holes + a.T;
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t warp_tot[2][kThreads / 32];
-    __shared__ uint64_t s_prefix, s_wand[kThreads / 32], s_wor[kThreads / 32];
-    __shared__ uint32_t s_rank;
-    __shared__ uint32_t s_unique;
+    const int nchunk = (a.slots + 31) / 32;
+    uint32_t* vals = reinterpret_cast<uint32_t*>(smem_raw);          // [slots] keys
+    uint32_t* hist = vals + nchunk * 32;                             // [kCopies][kBuckets]
+    uint32_t* comb = hist + kCopies * kBuckets;                      // [kBuckets]
+    uint32_t* hmask = comb + kBuckets;                               // [nchunk] hole bits
+    uint32_t* mmask = hmask + nchunk;                                // [nchunk] mover bits
+    // holes / movers (at most min(B, T) each) reuse the key buffer once the
+    // eviction bits are taken
+    int32_t* holes = reinterpret_cast<int32_t*>(vals);
+    int32_t* movers = holes + min(a.B, a.T);
+    __shared__ uint32_t gtot[kWarps], rout[3];
+    __shared__ uint32_t s_and[kWarps], s_or[kWarps];
+    __shared__ uint32_t wtot[2][kWarps];
+    __shared__ uint32_t s_pairs;
 
     // launched while the attention kernel still runs (programmatic dependent
     // launch): its column partials and the pool are read only after it has
@@ -63,6 +166,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     const int c = a.c, T = a.T, B = a.B;
     const int m = c + T;
     int32_t* pos = a.pos + (int64_t)u * a.slots;
+    if (m > B) {                                // the histograms start at zero
+        uint4* hv = reinterpret_cast<uint4*>(hist);
+        for (int e = tid; e < kCopies * kBuckets / 4; e += kThreads) hv[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
 
     // ---- 1-2. scores, positions, keys.  A thread issues every load of its
     // KU keys (the partials of up to TU query tiles each, and the positions)
@@ -74,7 +181,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     int32_t* spos = a.score_pos + (int64_t)u * a.m_pad;
     constexpr int KU = 2, TU = 12;
     const int n_rt = a.n_row_tiles;
-    uint64_t k_and = ~0ull, k_or = 0ull;
+    uint32_t k_and = ~0u, k_or = 0u;
     for (int j0 = tid; j0 < m; j0 += KU * kThreads) {
         float sv[KU];
         int32_t pv[KU];
@@ -110,8 +217,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
                 scores[j] = sv[q];
                 spos[j] = pv[q];
                 if (m > B) {
-                    const uint64_t k = a.window ? (uint64_t)(uint32_t)pv[q] << 32 : cand_key(sv[q], pv[q]);
-                    keys[j] = k;
+                    const uint32_t k = a.window ? (uint32_t)pv[q] : __float_as_uint(sv[q]);
+                    vals[j] = k;
                     k_and &= k;
                     k_or |= k;
                 }
@@ -123,160 +230,97 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
         return;
     }
 
-    // ---- 3. radix select of the E-th smallest key.  Bits every key shares
-    // are skipped (the score's sign and exponent bits usually): the first
-    // digit starts at the highest bit where keys differ.  Warps w and
-    // w + kHists share a histogram, so few increments of different warps
-    // collide on one address (with one histogram, every warp's increment
-    // of the one bucket all keys share serialised).
-    // AND and OR of all keys: per warp, then every warp folds the warps'
-    // partials itself (no second barrier)
-    auto and64 = [](uint64_t v) {
-        return ((uint64_t)__reduce_and_sync(0xffffffffu, (uint32_t)(v >> 32)) << 32) |
-               __reduce_and_sync(0xffffffffu, (uint32_t)v);
-    };
-    auto or64 = [](uint64_t v) {
-        return ((uint64_t)__reduce_or_sync(0xffffffffu, (uint32_t)(v >> 32)) << 32) |
-               __reduce_or_sync(0xffffffffu, (uint32_t)v);
-    };
+    // ---- 3. the cut of the E smallest keys
     {
-        const uint64_t wa = and64(k_and), wo = or64(k_or);
-        if (lane == 0) { s_wand[warp] = wa; s_wor[warp] = wo; }
+        const uint32_t wa = __reduce_and_sync(0xffffffffu, k_and);
+        const uint32_t wo = __reduce_or_sync(0xffffffffu, k_or);
+        if (lane == 0) { s_and[warp] = wa; s_or[warp] = wo; }
     }
-    for (int e = tid; e < kHists * 256; e += kThreads) whist[e] = 0u;
     __syncthreads();
-    const uint64_t k_all_and = and64(s_wand[lane]), k_all_or = or64(s_wor[lane]);
-    const uint64_t diff = k_all_and ^ k_all_or; // keys are distinct: diff != 0
-    const int top = 63 - __clzll((long long)diff);
-    uint64_t prefix = top < 63 ? (k_all_and & (~0ull << (top + 1))) : 0ull;
-    uint32_t rank = (uint32_t)(m - B);          // E: the E-th smallest key is evicted last
-    int hi = top;                               // highest bit of the current digit
-    while (hi >= 0) {
-        const int width = min(8, hi + 1);
-        const int shift = hi + 1 - width;
-        const uint32_t dmask = (1u << width) - 1u;
-        uint32_t* wh = whist + (warp % kHists) * 256;
-        for (int j0 = 0; j0 < m; j0 += kThreads) {
-            const int j = j0 + tid;
-            bool act = false;
-            uint32_t dig = 0;
-            if (j < m) {
-                const uint64_t k = keys[j];
-                act = hi == 63 || (k >> (hi + 1)) == (prefix >> (hi + 1));
-                dig = (uint32_t)(k >> shift) & dmask;
-            }
-            // one shared atomic per key: with the common high bits skipped the
-            // digits spread, and aggregating equal digits first (match_any)
-            // cost more than the few same-address conflicts it saves
-            if (act) atomicAdd(&wh[dig], 1u);
+    const RadixScratch rs{hist, comb, gtot, rout};
+    const uint32_t E = (uint32_t)(m - B);
+    const Cut cut = radix_cut([&](int j, uint32_t& k) { k = vals[j]; return true; }, m, (uint32_t)m, E,
+                              __reduce_and_sync(0xffffffffu, s_and[lane]),
+                              __reduce_or_sync(0xffffffffu, s_or[lane]), rs);
+    // equal scores on both sides of the cut (every bit compared, some of the
+    // boundary keys kept): of those, the lower positions are kept
+    Cut tie{0u, 0u, 0u, 0u};
+    const bool split_tie = cut.r != cut.cnt;
+    if (split_tie) {
+        auto tie_pos = [&](int j, uint32_t& k) {
+            k = (uint32_t)spos[j];
+            return vals[j] == cut.pre;
+        };
+        uint32_t ta = ~0u, to = 0u;
+        for (int j = tid; j < m; j += kThreads) {
+            uint32_t k;
+            if (tie_pos(j, k)) { ta &= k; to |= k; }
         }
+        ta = __reduce_and_sync(0xffffffffu, ta);
+        to = __reduce_or_sync(0xffffffffu, to);
+        __syncthreads();                        // s_and / s_or reads above are done
+        if (lane == 0) { s_and[warp] = ta; s_or[warp] = to; }
         __syncthreads();
-        if (tid < 256) {
-            uint32_t acc = 0;
-#pragma unroll
-            for (int w = 0; w < kHists; ++w) acc += whist[w * 256 + tid];
-            hist[tid] = acc;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            uint32_t h[8], run = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { h[e] = hist[lane * 8 + e]; run += h[e]; }
-            uint32_t incl = run;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += y;
-            }
-            const uint32_t excl = incl - run;
-            if (excl < rank && rank <= incl) {
-                uint32_t below = excl;
-                int b = 0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (below + h[e] >= rank) { b = e; break; }
-                    below += h[e];
-                }
-                s_prefix = prefix | ((uint64_t)(lane * 8 + b) << shift);
-                s_rank = rank - below;
-                s_unique = h[b] == 1u ? 1u : 0u;
-            }
-        } else {
-            // the histograms are read; clear them for the next digit
-            for (int e = tid - 32; e < kHists * 256; e += kThreads - 32) whist[e] = 0u;
-        }
-        __syncthreads();
-        prefix = s_prefix;
-        rank = s_rank;
-        if (s_unique) {
-            // one key has this prefix: it is the E-th smallest; fetch it whole
-            // and skip the remaining digits (usually the position digits)
-            const uint64_t pre = s_prefix >> shift;
-            __syncthreads();
-            for (int j = tid; j < m; j += kThreads)
-                if ((keys[j] >> shift) == pre) s_prefix = keys[j];
-            __syncthreads();
-            break;
-        }
-        hi -= width;
+        tie = radix_cut(tie_pos, m, cut.cnt, cut.cnt - cut.r,
+                        __reduce_and_sync(0xffffffffu, s_and[lane]),
+                        __reduce_or_sync(0xffffffffu, s_or[lane]), rs);
     }
-    const uint64_t kappa = s_prefix;            // E-th smallest key: evict <= kappa
+    auto evicted = [&](int j) -> bool {
+        const uint32_t hv = hi_bits(vals[j], cut.shift);
+        if (hv != cut.pre) return hv < cut.pre;
+        if (!split_tie) return true;
+        const uint32_t p = hi_bits((uint32_t)spos[j], tie.shift);     // kept: the lower positions
+        return !(p < tie.pre || (p == tie.pre && tie.r == tie.cnt));
+    };
 
-    // ---- 4. holes (slots < B evicted) and movers (slots >= B kept), slot
-    // order: a kept-bit per candidate (coalesced key reads), then each thread
-    // counts and lists the candidates of its contiguous chunk from the bits
-    for (int j0 = 0; j0 < m; j0 += kThreads) {
-        const int j = j0 + tid;
-        const uint32_t bits = __ballot_sync(0xffffffffu, j < m && keys[j] > kappa);
-        if (lane == 0 && j0 + warp * 32 < m) kept_bits[(j0 >> 5) + warp] = bits;
-    }
-    __syncthreads();                            // keys dead: holes / movers may overwrite them
-    auto kept_at = [&](int j) -> bool { return (kept_bits[j >> 5] >> (j & 31)) & 1u; };
-    const int per = (m + kThreads - 1) / kThreads;
-    const int j0 = tid * per, j1 = min(j0 + per, m);
+    // ---- 4. holes (slots < B evicted) and movers (slots >= B kept) in slot
+    // order: warp w takes the 32-slot chunks [w*cpw, (w+1)*cpw), a ballot per
+    // chunk and kind, then a scan over the warps' totals
+    const int nch = (m + 31) / 32;
+    const int cpw = (nch + kWarps - 1) / kWarps;
     uint32_t nh = 0, nm = 0;
-    for (int j = j0; j < j1; ++j) {
-        const bool kept = kept_at(j);
-        nh += (j < B && !kept);
-        nm += (j >= B && kept);
+    for (int q = warp * cpw; q < min(nch, (warp + 1) * cpw); ++q) {
+        const int j = q * 32 + lane;
+        const bool ev = j < m && evicted(j);
+        const uint32_t hb = __ballot_sync(0xffffffffu, ev && j < B);
+        const uint32_t mb = __ballot_sync(0xffffffffu, !ev && j < m && j >= B);
+        // surviving frame rows that stay in place get their position
+        if (!ev && j >= c && j < min(B, m)) pos[j] = a.pos_base + (j - c);
+        if (lane == 0) { hmask[q] = hb; mmask[q] = mb; }
+        nh += __popc(hb);
+        nm += __popc(mb);
     }
-    // block-wide exclusive scan of (nh, nm)
-    uint32_t ih = nh, im = nm;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        uint32_t yh = __shfl_up_sync(0xffffffffu, ih, off);
-        uint32_t ym = __shfl_up_sync(0xffffffffu, im, off);
-        if (lane >= off) { ih += yh; im += ym; }
-    }
-    if (lane == 31) { warp_tot[0][warp] = ih; warp_tot[1][warp] = im; }
-    __syncthreads();
+    if (lane == 0) { wtot[0][warp] = nh; wtot[1][warp] = nm; }
+    __syncthreads();                            // keys dead: holes / movers may overwrite them
     if (warp == 0) {
-        uint32_t th = warp_tot[0][lane], tm = warp_tot[1][lane];
+        const uint32_t th = wtot[0][lane], tm = wtot[1][lane];
         uint32_t ph = th, pm = tm;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            uint32_t yh = __shfl_up_sync(0xffffffffu, ph, off);
-            uint32_t ym = __shfl_up_sync(0xffffffffu, pm, off);
+            const uint32_t yh = __shfl_up_sync(0xffffffffu, ph, off);
+            const uint32_t ym = __shfl_up_sync(0xffffffffu, pm, off);
             if (lane >= off) { ph += yh; pm += ym; }
         }
-        warp_tot[0][lane] = ph - th;
-        warp_tot[1][lane] = pm - tm;
+        wtot[0][lane] = ph - th;
+        wtot[1][lane] = pm - tm;
+        if (lane == 31) {
+            // every hole gets a mover
+            s_pairs = min(ph, pm);
+            if (ph != pm) record_error(a.err, (uint32_t)STATEKV_E_DEVICE, kSiteSelect, ph * 65536u + pm);
+        }
     }
     __syncthreads();
-    uint32_t oh = warp_tot[0][warp] + ih - nh;
-    uint32_t om = warp_tot[1][warp] + im - nm;
-    for (int j = j0; j < j1; ++j) {
-        const bool kept = kept_at(j);
-        if (j < B && !kept) holes[oh++] = j;
-        if (j >= B && kept) movers[om++] = j;
-        // surviving frame rows that stay in place get their position
-        if (kept && j >= c && j < B) pos[j] = a.pos_base + (j - c);
-    }
-    // the last thread's end offsets are the totals; every hole gets a mover
-    __shared__ uint32_t s_pairs;
-    if (tid == kThreads - 1) {
-        s_pairs = min(oh, om);
-        if (oh != om) record_error(a.err, (uint32_t)STATEKV_E_DEVICE, kSiteSelect, oh * 65536u + om);
+    {
+        uint32_t oh = wtot[0][warp], om = wtot[1][warp];
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int q = warp * cpw; q < min(nch, (warp + 1) * cpw); ++q) {
+            const uint32_t hb = hmask[q], mb = mmask[q];
+            const int j = q * 32 + lane;
+            if ((hb >> lane) & 1u) holes[oh + __popc(hb & lt)] = j;
+            if ((mb >> lane) & 1u) movers[om + __popc(mb & lt)] = j;
+            oh += __popc(hb);
+            om += __popc(mb);
+        }
     }
     __syncthreads();
     const uint32_t np = s_pairs;
@@ -317,8 +361,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
 
 size_t select_smem_bytes(int slots, int T) {
     (void)T;                                    // holes / movers live in the key buffer
-    return (size_t)slots * sizeof(uint64_t) + (size_t)kHists * 256 * sizeof(uint32_t) +
-           (size_t)(slots + 31) / 32 * sizeof(uint32_t);
+    const size_t nchunk = (size_t)(slots + 31) / 32;
+    return nchunk * 32 * sizeof(uint32_t) + (size_t)(kCopies + 1) * kBuckets * sizeof(uint32_t) +
+           2 * nchunk * sizeof(uint32_t);
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
