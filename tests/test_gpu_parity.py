@@ -355,6 +355,44 @@ def test_cluster_multicast_is_bit_identical(cluster, monkeypatch):
                 assert raw_equal(x.cpu(), y.cpu()), f"C frame {n}"
 
 
+class _ZeroKeys:
+    """Frames of a source with every key set to zero (every logit 0)."""
+
+    def __init__(self, src):
+        self.src = src
+
+    def frame(self, n):
+        q, k, v = self.src.frame(n)
+        return q, np.zeros_like(k), v
+
+
+def test_exact_score_ties_keep_the_lower_positions():
+    """With K = 0 (so K' = 0 after RoPE) every logit is 0 and P is uniform
+    over each query row's visible keys: every compressed key and the frame's
+    key 0 (visible to every row) get bit-identical scores, the frame's later
+    keys strictly lower ones.  Once the state is full the cut (E = T
+    evictions) falls inside that tied group -- keys 1..T-1 plus one of the
+    tied keys -- and the tie rule (the lower position wins) keeps the
+    compressed keys: C holds positions 0..B-1 for ever.  Checked exactly, with
+    no near-tie allowance."""
+    sh = _small("ties", q_heads=4, kv_heads=2, layers=2, frames=7)
+    st = Stepper(sh)
+    st.src = _ZeroKeys(st.src)
+    T, B = sh.frame_tokens, sh.budget
+    for n in range(sh.frames):
+        c = min(n * T, B)
+        st.step(n)
+        for l in range(sh.layers):
+            sc, _, m = st.h.scores(0, l)
+            _, _, npos, ncnt = st.h.compressed(0, l)
+            for hk in range(sh.kv_heads):
+                s = sc[hk, :m].cpu().numpy()
+                assert (s[:c + 1] == s[0]).all(), f"frame {n} layer {l} head {hk}: tied scores differ"
+                assert (s[c + 1:] < s[0]).all(), f"frame {n} layer {l} head {hk}: frame key above the tie"
+                kept = np.sort(npos[hk, :ncnt].cpu().numpy().astype(np.int64))
+                np.testing.assert_array_equal(kept, np.arange(min(B, (n + 1) * T)))
+
+
 def test_window_policy_keeps_the_most_recent_tokens():
     """The sliding-window baseline on the same kernels: every step checked,
     through the fill and well past it."""
