@@ -32,8 +32,9 @@
 namespace statekv {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+// CTA size: 1024 threads, or 512 (two CTAs per SM) when the units are more
+// than the SMs, so that every unit's CTA starts at once
+constexpr int kMaxWarps = 32;
 constexpr int kDigit = 11;                      // radix digit width
 constexpr int kBuckets = 1 << kDigit;
 constexpr int kCopies = 4;                      // histogram copies: warp w counts into w % kCopies
@@ -52,14 +53,14 @@ __device__ __forceinline__ uint32_t hi_bits(uint32_t k, uint32_t shift) {
 struct RadixScratch {
     uint32_t* hist;                             // [kCopies][kBuckets], zero on entry and exit
     uint32_t* comb;                             // [kBuckets] the copies' sum
-    uint32_t* gtot;                             // [kWarps] per 64-bucket group
+    uint32_t* gtot;                             // [32] per 64-bucket group
     uint32_t* out;                              // [3] bucket, rank in it, its count
 };
 
 // The cut of the R smallest among the n active keys (1 <= R <= n; key_of(j,
 // k) says whether candidate j is active and sets its key); k_and / k_or are
 // the AND and OR of the active keys: their common high bits need no pass.
-template <class KeyOf>
+template <int NT, class KeyOf>
 __device__ Cut radix_cut(const KeyOf& key_of, int m, uint32_t n, uint32_t R, uint32_t k_and,
                          uint32_t k_or, const RadixScratch& rs) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -73,13 +74,14 @@ __device__ Cut radix_cut(const KeyOf& key_of, int m, uint32_t n, uint32_t R, uin
         const uint32_t w = min((uint32_t)kDigit, q.shift), sh = q.shift - w;
         const uint32_t dmask = (1u << w) - 1u;
         uint32_t* h = rs.hist + (warp % kCopies) * kBuckets;
-        for (int j = tid; j < m; j += kThreads) {
+        for (int j = tid; j < m; j += NT) {
             uint32_t k;
             if (key_of(j, k) && hi_bits(k, q.shift) == q.pre) atomicAdd(&h[(k >> sh) & dmask], 1u);
         }
         __syncthreads();
-        {   // bucket totals; warp g also sums group g (buckets 64g .. 64g+63)
-            const int b0 = warp * 64 + lane, b1 = b0 + 32;
+        // bucket totals, and per group of 64 buckets (32 groups, a warp each)
+        for (int grp = warp; grp < 32; grp += NT / 32) {
+            const int b0 = grp * 64 + lane, b1 = b0 + 32;
             uint32_t c0 = 0, c1 = 0;
 #pragma unroll
             for (int cp = 0; cp < kCopies; ++cp) {
@@ -89,7 +91,7 @@ __device__ Cut radix_cut(const KeyOf& key_of, int m, uint32_t n, uint32_t R, uin
             rs.comb[b0] = c0;
             rs.comb[b1] = c1;
             const uint32_t g = __reduce_add_sync(0xffffffffu, c0 + c1);
-            if (lane == 0) rs.gtot[warp] = g;
+            if (lane == 0) rs.gtot[grp] = g;
         }
         __syncthreads();
         if (warp == 0) {
@@ -124,7 +126,7 @@ __device__ Cut radix_cut(const KeyOf& key_of, int m, uint32_t n, uint32_t R, uin
         } else {
             // the copies are summed into comb: clear them for the next digit
             uint4* hv = reinterpret_cast<uint4*>(rs.hist);
-            for (int e = tid - 32; e < kCopies * kBuckets / 4; e += kThreads - 32)
+            for (int e = tid - 32; e < kCopies * kBuckets / 4; e += NT - 32)
                 hv[e] = make_uint4(0u, 0u, 0u, 0u);
         }
         __syncthreads();
@@ -136,7 +138,9 @@ __device__ Cut radix_cut(const KeyOf& key_of, int m, uint32_t n, uint32_t R, uin
     return q;
 }
 
-__global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
+    constexpr int NW = NT / 32;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int nchunk = (a.slots + 31) / 32;
     uint32_t* vals = reinterpret_cast<uint32_t*>(smem_raw);          // [slots] keys
@@ -148,9 +152,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     // eviction bits are taken
     int32_t* holes = reinterpret_cast<int32_t*>(vals);
     int32_t* movers = holes + min(a.B, a.T);
-    __shared__ uint32_t gtot[kWarps], rout[3];
-    __shared__ uint32_t s_and[kWarps], s_or[kWarps];
-    __shared__ uint32_t wtot[2][kWarps];
+    __shared__ uint32_t gtot[32], rout[3];
+    __shared__ uint32_t s_and[kMaxWarps], s_or[kMaxWarps];
+    __shared__ uint32_t wtot[2][kMaxWarps];
     __shared__ uint32_t s_pairs;
 
     // launched while the attention kernel still runs (programmatic dependent
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     int32_t* pos = a.pos + (int64_t)u * a.slots;
     if (m > B) {                                // the histograms start at zero
         uint4* hv = reinterpret_cast<uint4*>(hist);
-        for (int e = tid; e < kCopies * kBuckets / 4; e += kThreads) hv[e] = make_uint4(0u, 0u, 0u, 0u);
+        for (int e = tid; e < kCopies * kBuckets / 4; e += NT) hv[e] = make_uint4(0u, 0u, 0u, 0u);
     }
 
     // ---- 1-2. scores, positions, keys.  A thread issues every load of its
@@ -182,12 +186,12 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     constexpr int KU = 2, TU = 12;
     const int n_rt = a.n_row_tiles;
     uint32_t k_and = ~0u, k_or = 0u;
-    for (int j0 = tid; j0 < m; j0 += KU * kThreads) {
+    for (int j0 = tid; j0 < m; j0 += KU * NT) {
         float sv[KU];
         int32_t pv[KU];
 #pragma unroll
         for (int q = 0; q < KU; ++q) {
-            const int j = j0 + q * kThreads;
+            const int j = j0 + q * NT;
             sv[q] = 0.f;
             pv[q] = 0;
             if (j < m) pv[q] = j < c ? pos[j] : a.pos_base + (j - c);
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
             float part[KU][TU];
 #pragma unroll
             for (int q = 0; q < KU; ++q) {
-                const int j = j0 + q * kThreads;
+                const int j = j0 + q * NT;
 #pragma unroll
                 for (int tt = 0; tt < TU; ++tt)
                     part[q][tt] = (j < m && t0 + tt < n_rt)
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
         }
 #pragma unroll
         for (int q = 0; q < KU; ++q) {
-            const int j = j0 + q * kThreads;
+            const int j = j0 + q * NT;
             if (j < m) {
                 sv[q] *= a.inv_rows;
                 scores[j] = sv[q];
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
         }
     }
     if (m <= B) {                               // state not full: keep all
-        for (int j = c + tid; j < m; j += kThreads) pos[j] = a.pos_base + (j - c);
+        for (int j = c + tid; j < m; j += NT) pos[j] = a.pos_base + (j - c);
         return;
     }
 
@@ -239,9 +243,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     __syncthreads();
     const RadixScratch rs{hist, comb, gtot, rout};
     const uint32_t E = (uint32_t)(m - B);
-    const Cut cut = radix_cut([&](int j, uint32_t& k) { k = vals[j]; return true; }, m, (uint32_t)m, E,
-                              __reduce_and_sync(0xffffffffu, s_and[lane]),
-                              __reduce_or_sync(0xffffffffu, s_or[lane]), rs);
+    const Cut cut = radix_cut<NT>([&](int j, uint32_t& k) { k = vals[j]; return true; }, m, (uint32_t)m, E,
+                                  __reduce_and_sync(0xffffffffu, lane < NW ? s_and[lane] : ~0u),
+                                  __reduce_or_sync(0xffffffffu, lane < NW ? s_or[lane] : 0u), rs);
     // equal scores on both sides of the cut (every bit compared, some of the
     // boundary keys kept): of those, the lower positions are kept
     Cut tie{0u, 0u, 0u, 0u};
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
             return vals[j] == cut.pre;
         };
         uint32_t ta = ~0u, to = 0u;
-        for (int j = tid; j < m; j += kThreads) {
+        for (int j = tid; j < m; j += NT) {
             uint32_t k;
             if (tie_pos(j, k)) { ta &= k; to |= k; }
         }
@@ -261,9 +265,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
         __syncthreads();                        // s_and / s_or reads above are done
         if (lane == 0) { s_and[warp] = ta; s_or[warp] = to; }
         __syncthreads();
-        tie = radix_cut(tie_pos, m, cut.cnt, cut.cnt - cut.r,
-                        __reduce_and_sync(0xffffffffu, s_and[lane]),
-                        __reduce_or_sync(0xffffffffu, s_or[lane]), rs);
+        tie = radix_cut<NT>(tie_pos, m, cut.cnt, cut.cnt - cut.r,
+                            __reduce_and_sync(0xffffffffu, lane < NW ? s_and[lane] : ~0u),
+                            __reduce_or_sync(0xffffffffu, lane < NW ? s_or[lane] : 0u), rs);
     }
     auto evicted = [&](int j) -> bool {
         const uint32_t hv = hi_bits(vals[j], cut.shift);
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     // order: warp w takes the 32-slot chunks [w*cpw, (w+1)*cpw), a ballot per
     // chunk and kind, then a scan over the warps' totals
     const int nch = (m + 31) / 32;
-    const int cpw = (nch + kWarps - 1) / kWarps;
+    const int cpw = (nch + NW - 1) / NW;
     uint32_t nh = 0, nm = 0;
     for (int q = warp * cpw; q < min(nch, (warp + 1) * cpw); ++q) {
         const int j = q * 32 + lane;
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     if (lane == 0) { wtot[0][warp] = nh; wtot[1][warp] = nm; }
     __syncthreads();                            // keys dead: holes / movers may overwrite them
     if (warp == 0) {
-        const uint32_t th = wtot[0][lane], tm = wtot[1][lane];
+        const uint32_t th = lane < NW ? wtot[0][lane] : 0u, tm = lane < NW ? wtot[1][lane] : 0u;
         uint32_t ph = th, pm = tm;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     }
     __syncthreads();
     const uint32_t np = s_pairs;
-    for (uint32_t r = tid; r < np; r += kThreads) pos[holes[r]] = a.pos_base + (movers[r] - c);
+    for (uint32_t r = tid; r < np; r += NT) pos[holes[r]] = a.pos_base + (movers[r] - c);
 
     // ---- row moves (K and V), 16-byte vectors.  Holes are slots < B and
     // movers slots >= B, so no row is both read and written: each thread
@@ -336,12 +340,12 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectArgs a) {
     uint4* pk = reinterpret_cast<uint4*>((char*)a.pool_k + u * unit_bytes);
     uint4* pv = reinterpret_cast<uint4*>((char*)a.pool_v + u * unit_bytes);
     const int64_t total = (int64_t)np * vpr;
-    for (int64_t e0 = tid; e0 < total; e0 += MV * kThreads) {
+    for (int64_t e0 = tid; e0 < total; e0 += MV * NT) {
         uint4 vk[MV], vv[MV];
         int64_t dst[MV];
 #pragma unroll
         for (int q = 0; q < MV; ++q) {
-            const int64_t e = e0 + (int64_t)q * kThreads;
+            const int64_t e = e0 + (int64_t)q * NT;
             dst[q] = -1;
             if (e < total) {
                 const int r = (int)(e / vpr), w = (int)(e - (int64_t)r * vpr);
@@ -366,15 +370,16 @@ size_t select_smem_bytes(int slots, int T) {
            2 * nchunk * sizeof(uint32_t);
 }
 
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
+template <int NT>
+cudaError_t launch_select_nt(const SelectArgs& a, cudaStream_t st) {
     // a handle that never evicts never reaches the key buffer
     size_t smem = a.never_evicts ? 0 : select_smem_bytes(a.slots, a.T);
-    cudaError_t e = cudaFuncSetAttribute(select_kernel,
+    cudaError_t e = cudaFuncSetAttribute(select_kernel<NT>,
         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.U);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -382,7 +387,11 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, select_kernel, a);
+    return cudaLaunchKernelEx(&cfg, select_kernel<NT>, a);
+}
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
+    return a.U > a.num_sms ? launch_select_nt<512>(a, st) : launch_select_nt<1024>(a, st);
 }
 
 }  // namespace statekv

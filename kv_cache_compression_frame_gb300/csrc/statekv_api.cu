@@ -262,6 +262,7 @@ int run_back(statekv_handle* h, cudaStream_t st) {
     sa.inv_rows = (float)(1.0 / ((double)h->G * T));
     sa.window = c.select_policy == STATEKV_SELECT_WINDOW;
     sa.never_evicts = (int64_t)c.budget >= (int64_t)c.max_frames * T;
+    sa.num_sms = h->num_sms;
     cudaError_t e = timed(h, STATEKV_KERNEL_SELECT, st, [&] { return launch_select(sa, st); });
     if (e != cudaSuccess) return STATEKV_E_CUDA;
 

@@ -82,6 +82,7 @@ struct SelectArgs {
     float inv_rows;       // 1 / (G*T)
     int32_t window;       // 1: keep the B most recent tokens instead of Top-B
     int32_t never_evicts; // B >= every pool size this handle can reach
+    int32_t num_sms;      // SMs of the device (sets the CTA size)
 };
 
 cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st);
