@@ -26,6 +26,9 @@ using namespace statekv;
 
 namespace {
 
+// copy streams per direction of the batched host entry point
+constexpr int kCopyWays = 4;
+
 struct PendingEvent {
     int kernel;
     cudaEvent_t start, stop;
@@ -72,10 +75,11 @@ struct statekv_handle {
     // entry point (streams and events are created on its first call)
     void* stage2_q = nullptr; void* stage2_k = nullptr; void* stage2_v = nullptr;
     void* stage2_o = nullptr;
-    // two copy streams per direction: one copy stream moved ~100 GB/s, less
-    // than a frame's 29 MB in per frame time needs
-    cudaStream_t s_in[2] = {}, s_out[2] = {};
-    cudaEvent_t ev_entry = nullptr, ev_in[2][2] = {}, ev_front[2] = {}, ev_out[2][2] = {};
+    // kCopyWays copy streams per direction: one copy stream moved ~100 GB/s,
+    // less than a frame's inputs per frame time need
+    cudaStream_t s_in[kCopyWays] = {}, s_out[kCopyWays] = {};
+    cudaEvent_t ev_entry = nullptr, ev_in[2][kCopyWays] = {}, ev_front[2] = {},
+                ev_out[2][kCopyWays] = {};
     TcMaps tc{};                        // TMA views for the bf16 attention kernel
 
     bool profiling = false;
@@ -100,12 +104,15 @@ struct statekv_handle {
 namespace {
 
 void destroy_pipeline(statekv_handle* h) {
-    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0][0], &h->ev_in[0][1], &h->ev_in[1][0],
-                           &h->ev_in[1][1], &h->ev_front[0], &h->ev_front[1], &h->ev_out[0][0],
-                           &h->ev_out[0][1], &h->ev_out[1][0], &h->ev_out[1][1]})
+    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_front[0], &h->ev_front[1]})
         if (*e) { cudaEventDestroy(*e); *e = nullptr; }
-    for (cudaStream_t* st : {&h->s_in[0], &h->s_in[1], &h->s_out[0], &h->s_out[1]})
-        if (*st) { cudaStreamDestroy(*st); *st = nullptr; }
+    for (int sl = 0; sl < 2; ++sl)
+        for (int j = 0; j < kCopyWays; ++j)
+            for (cudaEvent_t* e : {&h->ev_in[sl][j], &h->ev_out[sl][j]})
+                if (*e) { cudaEventDestroy(*e); *e = nullptr; }
+    for (int j = 0; j < kCopyWays; ++j)
+        for (cudaStream_t* st : {&h->s_in[j], &h->s_out[j]})
+            if (*st) { cudaStreamDestroy(*st); *st = nullptr; }
 }
 
 void free_all(statekv_handle* h) {
@@ -418,12 +425,15 @@ namespace {
 bool ensure_pipeline(statekv_handle* h) {
     if (h->s_in[0]) return true;
     bool ok = true;
-    for (cudaStream_t* st : {&h->s_in[0], &h->s_in[1], &h->s_out[0], &h->s_out[1]})
-        ok = ok && cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) == cudaSuccess;
-    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_in[0][0], &h->ev_in[0][1], &h->ev_in[1][0],
-                           &h->ev_in[1][1], &h->ev_front[0], &h->ev_front[1], &h->ev_out[0][0],
-                           &h->ev_out[0][1], &h->ev_out[1][0], &h->ev_out[1][1]})
+    for (int j = 0; j < kCopyWays; ++j)
+        for (cudaStream_t* st : {&h->s_in[j], &h->s_out[j]})
+            ok = ok && cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* e : {&h->ev_entry, &h->ev_front[0], &h->ev_front[1]})
         ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    for (int sl = 0; sl < 2; ++sl)
+        for (int j = 0; j < kCopyWays; ++j)
+            for (cudaEvent_t* e : {&h->ev_in[sl][j], &h->ev_out[sl][j]})
+                ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         destroy_pipeline(h);
         cudaGetLastError();
@@ -433,12 +443,12 @@ bool ensure_pipeline(statekv_handle* h) {
 
 }  // namespace
 
-// Frames i = 0..F-1, staging slot i & 1; each copy is split over two streams
-// (j = 0, 1) of each direction:
-//   s_in[j] : [wait front(i-2)] H2D part j of q,k,v(i) -> slot     record ev_in[slot][j]
+// Frames i = 0..F-1, staging slot i & 1.  Each direction's bytes of a frame
+// are cut into kCopyWays equal ranges (256-byte aligned), one per stream j:
+//   s_in[j] : [wait front(i-2)] H2D range j of q|k|v(i) -> slot  record ev_in[slot][j]
 //   st      : front(i) (RoPE, attention)                         record ev_front[slot]
-//   s_out[j]: wait ev_front[slot]  D2H part j of o(i) <- slot       record ev_out[slot][j]
-//   st      : wait ev_in[next slot], [wait ev_out[next slot] of frame i-1],
+//   s_out[j]: wait ev_front[slot]  D2H range j of o(i) <- slot    record ev_out[slot][j]
+//   st      : wait ev_in[next slot][*], [wait ev_out[next slot][*] of frame i-1],
 //             back(i) (selection)
 // so the copies of frames i+1 (in) and i (out) overlap the step of frame
 // i, and the waits sit between the attention and the selection, never
@@ -459,32 +469,39 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
     void* sk[2] = {h->stage_k, h->stage2_k};
     void* sv[2] = {h->stage_v, h->stage2_v};
     void* so[2] = {h->stage_o, h->stage2_o};
-    // input part 0: the first qa bytes of q; part 1: the rest of q, k and v
-    const size_t qa = std::min(qb, ((qb + 2 * kvb) / 2 + 255) / 256 * 256);
-    const size_t oa = (qb / 2 + 255) / 256 * 256;      // output part 0: o[0, oa)
+    // range j of n bytes: [cut(n, j), cut(n, j + 1))
+    auto cut = [](size_t n, int j) {
+        return j >= kCopyWays ? n : std::min(n, (n * (size_t)j / kCopyWays + 255) / 256 * 256);
+    };
     auto ok = [](cudaError_t e) { return e == cudaSuccess; };
     if (!ok(cudaEventRecord(h->ev_entry, st))) return STATEKV_E_CUDA;
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < kCopyWays; ++j)
         if (!ok(cudaStreamWaitEvent(h->s_in[j], h->ev_entry, 0)) ||
             !ok(cudaStreamWaitEvent(h->s_out[j], h->ev_entry, 0)))
             return STATEKV_E_CUDA;
     auto h2d = [&](int32_t i) -> bool {
         const int sl = i & 1;
-        const char* qi = static_cast<const char*>(q) + (size_t)i * qb;
-        const char* ki = static_cast<const char*>(k) + (size_t)i * kvb;
-        const char* vi = static_cast<const char*>(v) + (size_t)i * kvb;
-        char* dq = static_cast<char*>(sq[sl]);
-        for (int j = 0; j < 2; ++j)
+        // the frame's inputs as one byte range [0, qb + 2 kvb): q, then k, then v
+        const char* src[3] = {static_cast<const char*>(q) + (size_t)i * qb,
+                              static_cast<const char*>(k) + (size_t)i * kvb,
+                              static_cast<const char*>(v) + (size_t)i * kvb};
+        char* dst[3] = {static_cast<char*>(sq[sl]), static_cast<char*>(sk[sl]),
+                        static_cast<char*>(sv[sl])};
+        const size_t off[4] = {0, qb, qb + kvb, qb + 2 * kvb};
+        for (int j = 0; j < kCopyWays; ++j) {
             if (i >= 2 && !ok(cudaStreamWaitEvent(h->s_in[j], h->ev_front[sl], 0))) return false;
-        return ok(cudaMemcpyAsync(dq, qi, qa, cudaMemcpyHostToDevice, h->s_in[0])) &&
-               ok(cudaEventRecord(h->ev_in[sl][0], h->s_in[0])) &&
-               (qa == qb || ok(cudaMemcpyAsync(dq + qa, qi + qa, qb - qa, cudaMemcpyHostToDevice,
-                                               h->s_in[1]))) &&
-               ok(cudaMemcpyAsync(sk[sl], ki, kvb, cudaMemcpyHostToDevice, h->s_in[1])) &&
-               ok(cudaMemcpyAsync(sv[sl], vi, kvb, cudaMemcpyHostToDevice, h->s_in[1])) &&
-               ok(cudaEventRecord(h->ev_in[sl][1], h->s_in[1])) &&
-               ok(cudaStreamWaitEvent(st, h->ev_in[sl][0], 0)) &&
-               ok(cudaStreamWaitEvent(st, h->ev_in[sl][1], 0));
+            const size_t lo = cut(off[3], j), hi = cut(off[3], j + 1);
+            for (int t = 0; t < 3; ++t) {
+                const size_t a = std::max(lo, off[t]), b = std::min(hi, off[t + 1]);
+                if (b > a && !ok(cudaMemcpyAsync(dst[t] + (a - off[t]), src[t] + (a - off[t]), b - a,
+                                                 cudaMemcpyHostToDevice, h->s_in[j])))
+                    return false;
+            }
+            if (!ok(cudaEventRecord(h->ev_in[sl][j], h->s_in[j])) ||
+                !ok(cudaStreamWaitEvent(st, h->ev_in[sl][j], 0)))
+                return false;
+        }
+        return true;
     };
     if (!h2d(0)) return STATEKV_E_CUDA;
     for (int32_t i = 0; i < frames; ++i) {
@@ -494,8 +511,8 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
         if (!ok(cudaEventRecord(h->ev_front[sl], st))) return STATEKV_E_CUDA;
         char* oi = static_cast<char*>(o) + (size_t)i * qb;
         const char* ds = static_cast<const char*>(so[sl]);
-        for (int j = 0; j < 2; ++j) {
-            const size_t b0 = j ? oa : 0, b1 = j ? qb : oa;
+        for (int j = 0; j < kCopyWays; ++j) {
+            const size_t b0 = cut(qb, j), b1 = cut(qb, j + 1);
             if (!ok(cudaStreamWaitEvent(h->s_out[j], h->ev_front[sl], 0)) ||
                 (b1 > b0 && !ok(cudaMemcpyAsync(oi + b0, ds + b0, b1 - b0, cudaMemcpyDeviceToHost,
                                                 h->s_out[j]))) ||
@@ -505,7 +522,7 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
         if (i + 1 < frames) {
             if (!h2d(i + 1)) return STATEKV_E_CUDA;
             // attention(i+1) rewrites the output slot of frame i-1
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < kCopyWays; ++j)
                 if (i >= 1 && !ok(cudaStreamWaitEvent(st, h->ev_out[(i + 1) & 1][j], 0)))
                     return STATEKV_E_CUDA;
         }
@@ -513,7 +530,7 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
         if (r != STATEKV_OK) return r;
     }
     for (int s2 = 0; s2 < 2 && s2 < frames; ++s2)
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < kCopyWays; ++j)
             if (!ok(cudaStreamWaitEvent(st, h->ev_out[(frames - 1 - s2) & 1][j], 0)))
                 return STATEKV_E_CUDA;
     return STATEKV_OK;
