@@ -194,8 +194,9 @@ int statekv_prefill_frame_host(statekv_handle* h, const void* q_host,
  *   q, o : [frames][S][L][Hq][T][d]      k, v : [frames][S][L][Hkv][T][d]
  * The same computation as `frames` calls of statekv_prefill_frame_host, but
  * the copies overlap the device work: the handle holds two staging slots,
- * and on two side streams of its own it copies frame i+1 in and frame i-1
- * out while frame i runs on cuda_stream.  The whole batch is ordered on
+ * and on side streams of its own (four per direction, each copying a quarter
+ * of a frame's bytes) it copies frame i+1 in and frame i-1 out while frame i
+ * runs on cuda_stream.  The whole batch is ordered on
  * cuda_stream like a single call: the side streams first wait for the work
  * already enqueued there, and cuda_stream waits for the last copy out, so
  * every o frame is valid (and q/k/v may be reused) once the stream passes
