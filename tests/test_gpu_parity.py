@@ -422,6 +422,7 @@ def test_full_attention_beyond_the_selection_limit():
     (64, 6, 2, 3, 7),         # odd T, odd B
     (128, 3, 1, 129, 130),    # G*T = 387: a ragged fourth query tile, pool 259 rows
     (64, 2, 2, 33, 0),        # G = 1, per-frame attention only
+    (64, 4, 2, 16, 8),        # budget below a frame: holes and movers at most B each
 ])
 def test_odd_shapes_every_step(head_dim, q_heads, kv_heads, T, B):
     sh = _small("odd", q_heads=q_heads, kv_heads=kv_heads, head_dim=head_dim,
