@@ -22,10 +22,10 @@
 //      Evicted slots below B ("holes") are refilled by surviving rows at or
 //      above B ("movers"), paired in slot order; only those rows move
 //      (<= T rows of K and V per unit instead of rewriting all B).
-// Every step is written for 32 warps that share each sub-partition eight
-// ways: per-thread work is kept to a few instructions per key (32-bit keys,
-// warp ballots for the slot-ordered lists), since each one costs eight
-// issue slots.
+// Every step is written for a full SM of warps (one 1024-thread CTA or two
+// 512-thread ones: eight warps per sub-partition): per-thread work is kept to
+// a few instructions per key (32-bit keys, warp ballots for the slot-ordered
+// lists), since each one costs eight issue slots.
 #include "statekv_internal.cuh"
 #include "sm100_ptx.cuh"
 
