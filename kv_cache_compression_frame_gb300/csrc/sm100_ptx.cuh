@@ -34,7 +34,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(bar), "r"(bytes) : "memory");
 }
-// Like mbar_test, but a thread whose phase is not yet complete is suspended
+// Like mbar_poll, but a thread whose phase is not yet complete is suspended
 // in hardware (no issue slots used) until the phase completes or about
 // hint_ns nanoseconds pass; returns whether the phase completed.
 __device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
@@ -74,10 +74,6 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t ran
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-                 :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
 // Arrive on a barrier of another CTA of the cluster (address from
 // cluster_map), releasing this thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
@@ -93,15 +89,6 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
                  : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
-// true once the phase with the given parity has completed
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
 
 // ------------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -112,9 +99,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
 
 // --------------------------------------------------------------------- TMA
@@ -177,20 +161,11 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                  :: "r"(taddr), "r"(ncols) : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 in, fp32 acc)
-__device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a_desc,
-                                            uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-// The same MMAs with each shared-memory descriptor given as its two 32-bit
-// halves: the start-address field sits in the low half and never carries out
-// (shared addresses < 256 KB), so callers advance a descriptor along K with a
-// single 32-bit add instead of rebuilding it.
+// D[tmem] (+)= A * B, kind::f16 (bf16 in, fp32 accumulate), each
+// shared-memory descriptor given as its two 32-bit halves: the start-address
+// field sits in the low half and never carries out (shared addresses < 256
+// KB), so callers advance a descriptor along K with a single 32-bit add
+// instead of rebuilding it.
 __device__ __forceinline__ void umma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                            uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                            uint32_t accumulate) {
@@ -201,6 +176,8 @@ __device__ __forceinline__ void umma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint3
                  :: "r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc),
                     "r"(accumulate) : "memory");
 }
+// The same with A read from tensor memory (M x 16 bf16 per k-step, two bf16
+// per 32-bit column, even element low).
 __device__ __forceinline__ void umma_ts_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                            uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
     asm volatile("{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
@@ -266,17 +243,6 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (M x 16 bf16 per k-step)
-// read from tensor memory, two bf16 per 32-bit column, even element low.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem,
-                                            uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
 
 // 16 lanes x 32 columns: per repetition r (0..3) thread t receives
 // (lane t/4, columns 8r + 2(t%4) + {0,1}) in r[4r], r[4r+1] and the same
