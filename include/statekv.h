@@ -108,13 +108,8 @@ typedef struct statekv_handle statekv_handle;   /* opaque */
  * Limits: G*T <= 65536 query rows per unit; B + T <= 24576 unless
  * B >= max_frames*T (no eviction: then only memory bounds the pool);
  * positions must fit in int32.
- * Environment: STATEKV_ATTN_CLUSTER = 2 or 4, read by statekv_create (and by
- * statekv_attend_scores_static on every call), makes bf16 attention CTAs of
- * consecutive query tiles of one KV head share each K/V tile by TMA
- * multicast within a thread-block cluster of that size (fewer L2 reads,
- * coupled pipelines; results are bit-identical).  Unset or any other value:
- * one CTA per query tile, the measured-faster default.
- * With one CTA per query tile, the tiles of the last, partial wave (when it
+ * The bf16 attention runs one CTA per 128-row query tile; the tiles of the
+ * last, partial wave (when it
  * fills at most half the SMs after at least one full wave) are each
  * computed by two CTAs of a cluster, one half of the key tiles each, which
  * exchange their row log-sum-exps and output halves through distributed

@@ -115,7 +115,7 @@ extern "C" int statekv_attend_scores_static(
     cudaError_t e;
     if (dtype == STATEKV_BF16) {
         TcMaps maps;
-        if (!make_tc_maps(&maps, pool_k, pool_v, head_dim, pool_rows, units, (int)n_row_tiles))
+        if (!make_tc_maps(&maps, pool_k, pool_v, head_dim, pool_rows, units))
             return STATEKV_E_CUDA;
         e = launch_attention_tc(a, maps, st);
     } else {

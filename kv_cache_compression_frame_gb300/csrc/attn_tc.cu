@@ -48,9 +48,6 @@
 // softmax works on S(t) and never waits for the signal that S(t) was read
 // (that arrive sits in the same per-SMSP queue as the softmax's ex2 burst
 // and completes late); P never aliases S.
-// Clusters of CS CTAs (consecutive query tiles of one unit) share every K/V
-// tile: each CTA loads 128/CS of its rows and multicasts them; a stage is
-// refilled only after every CTA of the cluster released it.
 // Every mbarrier wait is bounded; on timeout the CTA records
 // STATEKV_E_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM, exits.
 #include <cudaTypedefs.h>
@@ -134,14 +131,11 @@ __device__ __forceinline__ TileRange tile_range(int row0, int GT, int T, int c) 
 // add each other's O columns at the end (through distributed shared memory).
 // The last, partial wave runs this way, so its tiles take about 60 % as long
 // on twice as many SMs, and start as soon as SMs free up in the wave before.
-template <int D, int CS, bool SPLIT>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(TcLayout<D>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, AttnArgs a) {
-    static_assert(!SPLIT || CS == 1, "split tiles do not multicast");
     using L = TcLayout<D>;
-    constexpr int SLICE = 128 / CS;                     // K/V rows loaded by each CTA
-    constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -149,23 +143,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rt = a.n_row_tiles;
-    const int n_slots = (n_rt + CS - 1) / CS * CS;       // row tiles padded to whole clusters
     const int pair = (int)(blockIdx.x >> 1);
     const bool coop = SPLIT && 2 * pair >= a.split_item0;
     const int half = coop ? (int)ptx::cluster_ctarank() : 0;
     const int item = coop ? a.split_item0 + (pair - a.split_item0 / 2) : (int)blockIdx.x;
-    const int u = item / n_slots;
-    const int mt = item - u * n_slots;
-    const int rank = CS > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int u = item / n_rt;
+    const int mt = item - u * n_rt;
     const TileRange me = tile_range(mt * 128, a.GT, a.T, a.c);
     // this CTA's key tiles: [t0, t0 + nt_mine) of the tile's [0, me.nt)
     const int t0 = coop && half ? me.nt / 2 : 0;
     const int nt_mine = coop ? (half ? me.nt - me.nt / 2 : me.nt / 2) : me.nt;
-    int nt_load = 0;                                    // key tiles the cluster streams
-    if (SPLIT) nt_load = nt_mine;
-    else
-        for (int r = 0; r < CS; ++r)
-            nt_load = max(nt_load, tile_range((mt - rank + r) * 128, a.GT, a.T, a.c).nt);
 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + L::OFF_MISC + 4);
@@ -175,11 +162,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::mbar_init(sy.bar(L::B_Q), L::SW);
         for (int s = 0; s < L::KS; ++s) {
             ptx::mbar_init(sy.bar(L::B_K_FULL + s), 1);
-            ptx::mbar_init(sy.bar(L::B_K_EMPTY + s), CS);   // one release per CTA
+            ptx::mbar_init(sy.bar(L::B_K_EMPTY + s), 1);
         }
         for (int s = 0; s < L::VS; ++s) {
             ptx::mbar_init(sy.bar(L::B_V_FULL + s), 1);
-            ptx::mbar_init(sy.bar(L::B_V_EMPTY + s), CS);
+            ptx::mbar_init(sy.bar(L::B_V_EMPTY + s), 1);
         }
         for (int b = 0; b < L::SB1; ++b) {
             ptx::mbar_init(sy.bar(L::B_S_FULL + b), 1);
@@ -207,9 +194,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // peers multicast into (or, split, write) this CTA's shared memory and
-    // arrive on its barriers: all of them must be initialised first
-    if (CS > 1 || coop) ptx::cluster_sync();
+    // a split tile's other half writes into this CTA's shared memory and
+    // arrives on its barriers: all of them must be initialised first
+    if (coop) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // set-up above may overlap the end of the RoPE kernel (programmatic
@@ -231,7 +218,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     // earlier S products into buffer b: the buffer may be overwritten once
     // every softmax warp loaded the last of them.  Phases follow from the
     // tile indices, so the two warps need no shared state.
-    auto issue_s = [&](int kt, int b, bool needed, int prev_uses) -> bool {
+    auto issue_s = [&](int kt, int b, int prev_uses) -> bool {
         constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false, false);
         // a K step of 16 bf16 (32 bytes) adds 2 to the start-address field,
         // a stage (TILE bytes) adds TILE >> 4; in TMEM a K step of Q is 8 columns
@@ -240,26 +227,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int s = kt % L::KS, j = kt / L::KS;
         if (!sy.wait(L::B_K_FULL + s, (uint32_t)(j & 1), kSiteKvFull)) return false;
         ptx::tc_fence_after();
-        if (needed && prev_uses > 0) {
+        if (prev_uses > 0) {
             if (!sy.wait(L::B_S_READ + b, (uint32_t)((prev_uses - 1) & 1), kSiteSEmpty)) return false;
             ptx::tc_fence_after();
         }
         if (ptx::elect_one()) {
-            if (needed) {
-                const uint32_t d = tmem + 128u * b;
-                const uint32_t kb = kb0 + (uint32_t)s * (L::TILE >> 4);
+            const uint32_t d = tmem + 128u * b;
+            const uint32_t kb = kb0 + (uint32_t)s * (L::TILE >> 4);
 #pragma unroll
-                for (int kc = 0; kc < L::KCH; ++kc)
+            for (int kc = 0; kc < L::KCH; ++kc)
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        ptx::umma_ts_lh(d, tmem + L::TM_Q + 32u * kc + 8u * ks,
-                                        kb + kc * (L::CHUNK >> 4) + 2 * ks, desc_hi, idesc_qk,
-                                        (kc | ks) ? 1u : 0u);
-                ptx::umma_commit(sy.bar(L::B_S_FULL + b));
-            }
-            // the stage is free once every CTA of the cluster is done with it
-            if (CS > 1) ptx::umma_commit_mc(sy.bar(L::B_K_EMPTY + s), kMask);
-            else ptx::umma_commit(sy.bar(L::B_K_EMPTY + s));
+                for (int ks = 0; ks < 4; ++ks)
+                    ptx::umma_ts_lh(d, tmem + L::TM_Q + 32u * kc + 8u * ks,
+                                    kb + kc * (L::CHUNK >> 4) + 2 * ks, desc_hi, idesc_qk,
+                                    (kc | ks) ? 1u : 0u);
+            ptx::umma_commit(sy.bar(L::B_S_FULL + b));
+            // the stage is free once this product has read it
+            ptx::umma_commit(sy.bar(L::B_K_EMPTY + s));
         }
         __syncwarp();
         return true;
@@ -282,16 +266,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 if (!sy.wait(empty, (uint32_t)(j & 1) ^ 1u, kSiteKvEmpty)) return false;
                 const uint32_t fb = sy.bar((is_v ? L::B_V_FULL : L::B_K_FULL) + s);
                 ptx::mbar_arrive_expect_tx(fb, L::TILE);
-                const uint32_t dst = (is_v ? sV : sK) + s * L::TILE + rank * SLICE * 128;
+                const uint32_t dst = (is_v ? sV : sK) + s * L::TILE;
                 const CUtensorMap* map = is_v ? &tm_v : &tm_k;
 #pragma unroll
-                for (int kc = 0; kc < L::KCH; ++kc) {
-                    if (CS > 1)
-                        ptx::tma_load_3d_mc(dst + kc * L::CHUNK, map, fb, kc * 64,
-                                            (t0 + t) * L::BN + rank * SLICE, u, kMask);
-                    else
-                        ptx::tma_load_3d(dst + kc * L::CHUNK, map, fb, kc * 64, (t0 + t) * L::BN, u);
-                }
+                for (int kc = 0; kc < L::KCH; ++kc)
+                    ptx::tma_load_3d(dst + kc * L::CHUNK, map, fb, kc * 64, (t0 + t) * L::BN, u);
                 if (is_v) ++vt; else ++kt;
                 return true;
             };
@@ -301,10 +280,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             // K(t+2) goes first; behind V(t), which waits for PV(t-2) to free
             // its stage, it arrived just in time for S(t+2) to enter the
             // tensor pipe ahead of PV(t) and delay it by a whole product
-            for (int t = 0; ok && t < nt_load; ++t) ok = load(t, false);
-            for (int t = 0; ok && t < min(2, nt_load); ++t) ok = load(t, false);
-            for (int t = 0; ok && t < nt_load; ++t) {
-                if (t + 2 < nt_load) ok = load(t + 2, false);
+            for (int t = 0; ok && t < nt_mine; ++t) ok = load(t, false);
+            for (int t = 0; ok && t < min(2, nt_mine); ++t) ok = load(t, false);
+            for (int t = 0; ok && t < nt_mine; ++t) {
+                if (t + 2 < nt_mine) ok = load(t + 2, false);
                 if (ok) ok = load(t, true);
             }
             // never leave a copy in flight into this CTA's shared memory: wait
@@ -322,17 +301,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::tc_fence_after();
         // sweep 1: three S buffers in rotation; this warp issues the even
         // tiles, the PV warp (idle until sweep 2) the odd ones
-        for (int t = 0; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < nt_mine, t / L::SB1);
+        for (int t = 0; ok && t < nt_mine; t += 2) ok = issue_s(t, t % L::SB1, t / L::SB1);
         // sweep 2: S buffers 0 and 1; S(t+2) waits only for S(t) to have
         // been loaded, so it is computed while the softmax works on S(t+1).
         // This warp now also consumes the K stages and S buffers the PV warp
         // used in sweep 1: it starts once that warp passed its last sweep-1
         // waits, or a parity wait here could match a phase two back
         if (ok) ok = sy.wait(L::B_S1_DONE, 0, kSiteSEmpty);
-        for (int t = 0; ok && t < nt_load; ++t) {
+        for (int t = 0; ok && t < nt_mine; ++t) {
             const int b = t & 1;
             const int s1_uses = nt_mine > b ? (nt_mine - 1 - b) / L::SB1 + 1 : 0;
-            ok = issue_s(nt_load + t, b, t < nt_mine, s1_uses + t / 2);
+            ok = issue_s(nt_mine + t, b, s1_uses + t / 2);
         }
         // all MMAs complete before TMEM is released
         if (ptx::elect_one()) ptx::umma_commit(sy.bar(L::B_DRAIN));
@@ -351,19 +330,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         // sweep 1: the odd S tiles (warp 1 issues the even ones)
         bool ok = sy.wait(L::B_Q, 0, kSiteQFull);
         ptx::tc_fence_after();
-        for (int t = 1; ok && t < nt_load; t += 2) ok = issue_s(t, t % L::SB1, t < nt_mine, t / L::SB1);
+        for (int t = 1; ok && t < nt_mine; t += 2) ok = issue_s(t, t % L::SB1, t / L::SB1);
         if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_S1_DONE));
         // O overlays sweep-1 S buffer 2: P(0) is written only after every
         // softmax warp finished sweep 1, so PV(0) waiting for P(0) is enough
-        for (int t = 0; ok && t < nt_load; ++t) {
+        for (int t = 0; ok && t < nt_mine; ++t) {
             const int vs = t % L::VS, jv = t / L::VS;
             if (!(ok = sy.wait(L::B_V_FULL + vs, (uint32_t)(jv & 1), kSiteKvFull))) break;
-            const bool mine = t < nt_mine;
             // each 64-key half of P(t) goes to the tensor pipe as soon as its
             // 8 warps wrote it, and is handed back as soon as its 4 MMAs are
             // done: the warps of one half refill it while the other half's
             // products still run
-            for (int h = 0; mine && h < 2; ++h) {
+            for (int h = 0; h < 2; ++h) {
                 if (!(ok = sy.wait(L::B_P_FULL + h, pv_par, kSitePFull))) break;
                 ptx::tc_fence_after();
                 if (ptx::elect_one()) {
@@ -382,12 +360,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 __syncwarp();
             }
             if (!ok) break;
-            if (ptx::elect_one()) {
-                if (CS > 1) ptx::umma_commit_mc(sy.bar(L::B_V_EMPTY + vs), kMask);
-                else ptx::umma_commit(sy.bar(L::B_V_EMPTY + vs));
-            }
+            if (ptx::elect_one()) ptx::umma_commit(sy.bar(L::B_V_EMPTY + vs));
             __syncwarp();
-            if (mine) {
+            {
                 pv_par ^= 1u;
                 // key column sums of P(t): the 4 lane quarters' partials (kept
                 // in L2 for the select kernel that reads them after this grid)
@@ -765,19 +740,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
 
     __syncthreads();
-    // no CTA leaves while a peer may still multicast into it or arrive on
-    // its barriers (every role above has drained its own traffic)
-    if (CS > 1 || coop) ptx::cluster_sync();
+    // no CTA leaves while its split-tile peer may still write into it or
+    // arrive on its barriers (every role above has drained its own traffic)
+    if (coop) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, L::TMEM_COLS);
     }
 }
 
-template <int D, int CS, bool SPLIT>
+template <int D, bool SPLIT>
 cudaError_t launch_grid(const AttnArgs& a, const TcMaps& m, cudaStream_t st, int grid) {
     using L = TcLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, CS, SPLIT>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -787,14 +762,14 @@ cudaError_t launch_grid(const AttnArgs& a, const TcMaps& m, cudaStream_t st, int
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = SPLIT ? 2 : CS;
+    attr[0].val.clusterDim.x = SPLIT ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, CS, SPLIT>, m.k, m.v, a);
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, SPLIT>, m.k, m.v, a);
 }
 
 // Query tiles run as a key-split pair: the tiles of the last, partial wave
@@ -813,22 +788,19 @@ int split_tiles(int items, int resident) {
     return (full > 0 && tail > 0 && 2 * tail <= resident) ? tail : 0;
 }
 
-template <int D, int CS>
+template <int D>
 cudaError_t launch_tc(const AttnArgs& a_in, const TcMaps& m, cudaStream_t st) {
-    const int n_slots = (a_in.n_row_tiles + CS - 1) / CS * CS;
-    const int items = a_in.U * n_slots;
-    if (CS > 1) return launch_grid<D, CS, false>(a_in, m, st, items);
+    const int items = a_in.U * a_in.n_row_tiles;
     AttnArgs a = a_in;
     int split = split_tiles(items, a.resident);
     if (split == 0) {
         a.split_item0 = items;
-        return launch_grid<D, 1, false>(a, m, st, items);
+        return launch_grid<D, false>(a, m, st, items);
     }
     // whole tiles go two per cluster: an even count
     if ((items - split) & 1) ++split;
     a.split_item0 = items - split;
-    cudaError_t e = launch_grid<D, 1, true>(a, m, st, a.split_item0 + 2 * split);
-    return e;
+    return launch_grid<D, true>(a, m, st, a.split_item0 + 2 * split);
 }
 
 }  // namespace
@@ -860,40 +832,15 @@ bool encode_view(CUtensorMap* m, const void* base, int d, int64_t rows, int64_t 
            CUDA_SUCCESS;
 }
 
-int tc_cluster_size(int n_row_tiles) {
-    // CTAs of a cluster are consecutive query tiles of one unit.  Sharing
-    // K/V tiles by multicast cuts L2 reads by the cluster size but couples
-    // the CTAs' pipelines; on GB300 one CTA per tile measured fastest, so
-    // clusters are opt-in (STATEKV_ATTN_CLUSTER = 2 or 4, read when the
-    // tensor maps are built).
-    int want = 1;
-    if (const char* e = getenv("STATEKV_ATTN_CLUSTER")) {
-        const int v = atoi(e);
-        if (v == 2 || v == 4) want = v;
-    }
-    while (want > 1 && n_row_tiles < want) want >>= 1;
-    return want;
-}
-
 bool make_tc_maps(TcMaps* m, const void* pool_k, const void* pool_v, int d, int64_t slots,
-                  int64_t units, int n_row_tiles) {
-    m->cs = tc_cluster_size(n_row_tiles);
-    const int kv_rows = 128 / m->cs;
-    return encode_view(&m->k, pool_k, d, slots, units, kv_rows) &&
-           encode_view(&m->v, pool_v, d, slots, units, kv_rows);
+                  int64_t units) {
+    return encode_view(&m->k, pool_k, d, slots, units, 128) &&
+           encode_view(&m->v, pool_v, d, slots, units, 128);
 }
 
 cudaError_t launch_attention_tc(const AttnArgs& a, const TcMaps& m, cudaStream_t st) {
-    if (a.d == 128) {
-        if (m.cs == 4) return launch_tc<128, 4>(a, m, st);
-        if (m.cs == 2) return launch_tc<128, 2>(a, m, st);
-        return launch_tc<128, 1>(a, m, st);
-    }
-    if (a.d == 64) {
-        if (m.cs == 4) return launch_tc<64, 4>(a, m, st);
-        if (m.cs == 2) return launch_tc<64, 2>(a, m, st);
-        return launch_tc<64, 1>(a, m, st);
-    }
+    if (a.d == 128) return launch_tc<128>(a, m, st);
+    if (a.d == 64) return launch_tc<64>(a, m, st);
     return cudaErrorInvalidValue;
 }
 

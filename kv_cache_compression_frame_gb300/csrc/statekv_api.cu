@@ -368,7 +368,7 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
         if (launch_rope_table(ta, nullptr) != cudaSuccess) { free_all(h); delete h; return STATEKV_E_CUDA; }
     }
     if (c.dtype == STATEKV_BF16 &&
-        !make_tc_maps(&h->tc, h->pool_k, h->pool_v, d, h->slots, h->U, h->n_row_tiles)) {
+        !make_tc_maps(&h->tc, h->pool_k, h->pool_v, d, h->slots, h->U)) {
         free_all(h); delete h; return STATEKV_E_CUDA;
     }
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c.device) !=

@@ -87,16 +87,13 @@ struct SelectArgs {
 
 cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st);
 cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st, bool early);
-// TMA views of the attention kernel's operands and the cluster size they
-// were encoded for (K/V boxes hold 128 / cs rows: each CTA of a cluster
-// loads that share of a tile and multicasts it).
+// TMA views of the attention kernel's operands: K and V of the pool as
+// [units][slots][d], read in 128-row boxes.
 struct TcMaps {
     CUtensorMap k, v;
-    int cs;
 };
-int tc_cluster_size(int n_row_tiles);
 bool make_tc_maps(TcMaps* m, const void* pool_k, const void* pool_v, int d, int64_t slots,
-                  int64_t units, int n_row_tiles);
+                  int64_t units);
 cudaError_t launch_attention_tc(const AttnArgs& a, const TcMaps& maps, cudaStream_t st);
 cudaError_t launch_attention_simt(const AttnArgs& a, cudaStream_t st);
 

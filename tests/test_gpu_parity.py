@@ -329,32 +329,6 @@ def test_profile_kernels_brackets_only_the_chosen_kernel():
         st.h.profile_kernels("nope")
 
 
-@pytest.mark.parametrize("cluster", ["2", "4"])
-def test_cluster_multicast_is_bit_identical(cluster, monkeypatch):
-    """K/V tiles shared by TMA multicast across a cluster of query-tile CTAs
-    give exactly the one-CTA-per-tile results (same arithmetic per CTA)."""
-    sh = _small("cluster", q_heads=8, kv_heads=2, head_dim=128, frame_tokens=128,
-                budget=256, frames=4)            # G*T = 512 rows: 4 query tiles per unit
-    monkeypatch.delenv("STATEKV_ATTN_CLUSTER", raising=False)
-    ref = Stepper(sh)
-    monkeypatch.setenv("STATEKV_ATTN_CLUSTER", cluster)
-    mc = Stepper(sh)
-    for n in range(sh.frames):
-        o_ref = ref.run(n).cpu()
-        if n == sh.frames - 1:
-            mc.step(n)                           # and against the oracle once
-            o_mc = None
-        else:
-            o_mc = mc.run(n).cpu()
-        if o_mc is not None:
-            assert raw_equal(o_ref, o_mc), f"O frame {n}"
-        for l in range(sh.layers):
-            a, b = ref.h.compressed(0, l), mc.h.compressed(0, l)
-            assert a[3] == b[3]
-            for x, y in zip(a[:3], b[:3]):
-                assert raw_equal(x.cpu(), y.cpu()), f"C frame {n}"
-
-
 class _ZeroKeys:
     """Frames of a source with every key set to zero (every logit 0)."""
 
