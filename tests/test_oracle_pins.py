@@ -253,6 +253,98 @@ def check_topb_rank_definition(o=orc):
         assert list(pos[keep]) == sorted(pos[keep])
 
 
+def check_golden_alpha4_logit_temperature(o=orc):
+    """Hand-evaluated alpha = 4 step (tests/golden/yarn_alpha4_logit_d4.json):
+    the logit against a key at the query's own position is q.k * mscale^2 /
+    sqrt(d) (a common rotation preserves the inner product), and a zero key
+    gives logit 0, so P, O, the scores and the kept position are closed
+    forms in mscale = 0.1 ln 4 + 1.  Runs through StateKVOracle, so the
+    temperature is taken where the oracle itself takes it."""
+    g = _load("yarn_alpha4_logit_d4.json")
+    st = g["setup"]
+    cfg = _Cfg(q_heads=st["G"], kv_heads=1, head_dim=st["head_dim"], frame_tokens=st["T"],
+               budget=st["B"], rope_theta=st["theta"], rope_alpha=st["alpha"],
+               rope_orig_ctx=st["orig_ctx"], dtype=st["dtype"])
+    ref = o.StateKVOracle(cfg)
+    assert abs(ref.mscale ** 2 - g["mscale_squared"]) < 1e-9
+    q = np.array(st["q"], np.float64)[None, None, None]      # [S][L][Hq][T][d]
+    k = np.array(st["k"], np.float64)[None, None, None]
+    v = np.array(st["v"], np.float64)[None, None, None]
+    O, infos = ref.prefill_frame(q, k, v, keep_info=True)
+    tol = g["abs_tol"]
+    np.testing.assert_allclose(O[0, 0, 0], g["O"], rtol=0, atol=tol)
+    info = infos[(0, 0, 0)]
+    np.testing.assert_allclose(info["scores"], g["scores"], rtol=0, atol=tol)
+    np.testing.assert_array_equal(ref.units[(0, 0, 0)].comp_pos, g["kept_positions"])
+    # the probabilities themselves, through the unit-level attention
+    unit = o.UnitState(st["head_dim"])
+    omega, ms = o.rope_frequencies(st["head_dim"], st["theta"], st["alpha"], st["orig_ctx"])
+    _, info = o.prefill_unit_frame(unit, q[0, 0, 0:1], k[0, 0, 0], v[0, 0, 0], 0,
+                                   budget=st["B"], omega=omega,
+                                   scale=o.logit_scale(st["head_dim"], ms), dtype=st["dtype"])
+    np.testing.assert_allclose(info["P"][0], g["P"], rtol=0, atol=tol)
+
+
+def _per_head_causal(q_h, k_h, v_h, pos, theta, scale):
+    """Causal attention of one query head over one KV head's keys, one query
+    at a time (loops), with fp32-stored rotated q/k.  q_h, k_h, v_h: [T, d]
+    for a single frame at positions pos.  Returns (O [T, d], P [T, T])."""
+    T, d = q_h.shape
+    qr = _complex_rope(q_h, pos, theta).astype(np.float32).astype(np.float64)
+    kr = _complex_rope(k_h, pos, theta).astype(np.float32).astype(np.float64)
+    out = np.zeros((T, d))
+    P = np.zeros((T, T))
+    for i in range(T):
+        logits = [float(np.dot(qr[i], kr[j])) * scale for j in range(i + 1)]
+        mx = max(logits)
+        w = [math.exp(a - mx) for a in logits]
+        tot = sum(w)
+        for j in range(i + 1):
+            P[i, j] = w[j] / tot
+            out[i] += P[i, j] * v_h[j]
+    return out, P
+
+
+def check_gqa_head_grouping(o=orc):
+    """Query head j attends with KV head j // G (G = Hq / Hkv consecutive
+    query heads share a KV head), and the scores of KV head h average the P
+    of exactly those G heads.  StateKVOracle on Hq = 4, Hkv = 2 against
+    per-query-head brute force: full causal attention over the whole stream
+    (B covers every frame), and the first frame's scores."""
+    Hq, Hkv, T, d, N = 4, 2, 3, 8, 3
+    G = Hq // Hkv
+    theta = 1e4
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((N, 1, 1, Hq, T, d))
+    k = rng.standard_normal((N, 1, 1, Hkv, T, d))
+    v = rng.standard_normal((N, 1, 1, Hkv, T, d))
+    cfg = _Cfg(q_heads=Hq, kv_heads=Hkv, head_dim=d, frame_tokens=T, budget=N * T,
+               rope_theta=theta, dtype="f32")
+    ref = o.StateKVOracle(cfg)
+    outs = [ref.prefill_frame(q[n], k[n], v[n]) for n in range(N)]
+    for j in range(Hq):
+        h = j // G
+        want = _brute_full_causal(q[:, 0, 0, j][:, None].transpose(0, 2, 1, 3).reshape(N * T, 1, d),
+                                  k[:, 0, 0, h].reshape(N * T, d), v[:, 0, 0, h].reshape(N * T, d),
+                                  theta, 1.0 / math.sqrt(d), 1)[:, 0]
+        got = np.concatenate([outs[n][0, 0, j] for n in range(N)])
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+    # scores of the first frame (no compressed keys): per KV head, the mean
+    # over its G query heads and T rows of each head's P
+    cfg2 = _Cfg(q_heads=Hq, kv_heads=Hkv, head_dim=d, frame_tokens=T, budget=1,
+                rope_theta=theta, dtype="f32")
+    ref2 = o.StateKVOracle(cfg2)
+    _, infos = ref2.prefill_frame(q[0], k[0], v[0], keep_info=True)
+    pos = np.arange(T)
+    for h in range(Hkv):
+        acc = np.zeros(T)
+        for j in range(h * G, (h + 1) * G):
+            _, P = _per_head_causal(q[0, 0, 0, j], k[0, 0, 0, h], v[0, 0, 0, h], pos, theta,
+                                    1.0 / math.sqrt(d))
+            acc += P.sum(0)
+        np.testing.assert_allclose(infos[(0, 0, h)]["scores"], acc / (G * T), rtol=0, atol=1e-12)
+
+
 # ----------------------------------------------------------------- the tests
 def test_golden_zero_keys():
     check_golden_zero_keys()
@@ -280,6 +372,14 @@ def test_zero_budget_matches_sdpa():
 
 def test_topb_rank_definition():
     check_topb_rank_definition()
+
+
+def test_golden_alpha4_logit_temperature():
+    check_golden_alpha4_logit_temperature()
+
+
+def test_gqa_head_grouping():
+    check_gqa_head_grouping()
 
 
 def test_yarn_golden_and_limits():
@@ -476,7 +576,8 @@ def _mut_pv_transposed_heads(monkeypatch):
 _CHECKS = [check_golden_zero_keys, check_rope_complex,
            check_full_sa_when_budget_covers_all, check_decode_is_full_causal_over_the_stream,
            check_window_policy_is_a_sliding_window,
-           check_zero_budget_is_per_frame_causal, check_topb_rank_definition]
+           check_zero_budget_is_per_frame_causal, check_topb_rank_definition,
+           check_golden_alpha4_logit_temperature, check_gqa_head_grouping]
 
 
 def _mut_decode_reads_compressed(monkeypatch):
@@ -513,11 +614,44 @@ def _mut_window_keeps_oldest(monkeypatch):
     monkeypatch.setattr(orc, "select_window", bad)
 
 
+def _mut_mscale_not_squared(monkeypatch):
+    # the YaRN temperature applied once instead of squared
+    monkeypatch.setattr(orc, "logit_scale", lambda d, ms: ms / math.sqrt(d))
+
+
+def _mut_no_temperature(monkeypatch):
+    # alpha != 1 without the YaRN temperature: the plain 1/sqrt(d)
+    monkeypatch.setattr(orc, "logit_scale", lambda d, ms: 1.0 / math.sqrt(d))
+
+
+def _mut_heads_interleaved(monkeypatch):
+    # query head j paired with KV head j % Hkv instead of j // G
+    class Bad(orc.StateKVOracle):
+        def prefill_frame(self, q, k, v, keep_info=False):
+            cfg = self.cfg
+            O = np.zeros(np.shape(q), np.float64)
+            infos = {}
+            for (s, l, h), st in self.units.items():
+                heads = list(range(h, cfg.q_heads, cfg.kv_heads))
+                o_, info = orc.prefill_unit_frame(
+                    st, np.asarray(q[s][l])[heads], k[s][l][h], v[s][l][h], self.n,
+                    budget=cfg.budget, omega=self.omega, scale=self.scale,
+                    dtype=cfg.dtype, position_offset=self.offset)
+                O[s, l, heads] = o_
+                if keep_info:
+                    info.pop("P")
+                    infos[(s, l, h)] = info
+            self.n += 1
+            return (O, infos) if keep_info else O
+    monkeypatch.setattr(orc, "StateKVOracle", Bad)
+
+
 @pytest.mark.parametrize("mutation", [
     _mut_mask_offbyone, _mut_window_keeps_oldest, _mut_score_visible_mean, _mut_tiebreak_high,
     _mut_rope_sign, _mut_rope_freq_index, _mut_no_scale,
     _mut_pv_transposed_heads, _mut_decode_reads_compressed,
-    _mut_decode_position_restart])
+    _mut_decode_position_restart, _mut_mscale_not_squared, _mut_no_temperature,
+    _mut_heads_interleaved])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     mutation(monkeypatch)
     caught = 0
