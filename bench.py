@@ -143,46 +143,66 @@ def _traffic(kernel: str):
 
 
 # --------------------------------------------------------------- CPU oracle
-def _oracle_frame_sample(sh, layers: int, seed: int = 1):
-    """Time the oracle on `layers` layers of one steady-state frame (the
-    compressed state full, c = B).  Returns seconds."""
-    import numpy as np
-    import oracle.statekv_oracle as orc
-    from synth import FrameSource
-    src = FrameSource(sh)
-    omega, ms = orc.rope_frequencies(sh.head_dim, sh.rope_theta, sh.rope_alpha, sh.rope_orig_ctx)
-    scale = orc.logit_scale(sh.head_dim, ms)
-    rng = np.random.default_rng(seed)
-    n = sh.budget // sh.frame_tokens            # first frame with a full state
-    G, B, d = sh.group, sh.budget, sh.head_dim
-    states = []
-    for _ in range(layers * sh.kv_heads):       # synthetic full state (not timed)
-        st = orc.UnitState(d)
-        pos = np.arange(B, dtype=np.int64)
-        st.comp_k = orc.round_to_storage(orc.rope_rotate(rng.standard_normal((B, d)), pos, omega), sh.dtype)
-        st.comp_v = orc.round_to_storage(rng.standard_normal((B, d)), sh.dtype)
-        st.comp_pos = pos
-        states.append(st)
-    inputs = [src.layer_frame(0, l, n) for l in range(layers)]
-    t0 = time.perf_counter()
-    i = 0
-    for l in range(layers):
-        q, k, v = inputs[l]
-        for hk in range(sh.kv_heads):
-            orc.prefill_unit_frame(states[i], q[hk * G:(hk + 1) * G], k[hk], v[hk], n,
-                                   budget=B, omega=omega, scale=scale, dtype=sh.dtype)
-            i += 1
-    return time.perf_counter() - t0
+class _OracleSample:
+    """The oracle on `layers` layers (all their KV heads) of a stream in steady
+    state: the compressed state starts full (B synthetic rows at positions
+    0..B-1, rotated and storage-rounded like real keys; built untimed), and
+    each frame() call runs the next frame n = B/T, B/T + 1, ... through the
+    oracle's own step, so the state evolves by its own selection."""
+
+    def __init__(self, sh, layers: int, seed: int = 1):
+        import numpy as np
+        import oracle.statekv_oracle as orc
+        from synth import FrameSource
+        self.orc, self.sh, self.layers = orc, sh, layers
+        self.src = FrameSource(sh)
+        self.omega, ms = orc.rope_frequencies(sh.head_dim, sh.rope_theta, sh.rope_alpha,
+                                              sh.rope_orig_ctx)
+        self.scale = orc.logit_scale(sh.head_dim, ms)
+        self.n = sh.budget // sh.frame_tokens       # first frame with a full state
+        rng = np.random.default_rng(seed)
+        B, d = sh.budget, sh.head_dim
+        self.states = []
+        for _ in range(layers * sh.kv_heads):
+            st = orc.UnitState(d)
+            pos = np.arange(B, dtype=np.int64)
+            st.comp_k = orc.round_to_storage(orc.rope_rotate(rng.standard_normal((B, d)), pos,
+                                                             self.omega), sh.dtype)
+            st.comp_v = orc.round_to_storage(rng.standard_normal((B, d)), sh.dtype)
+            st.comp_pos = pos
+            self.states.append(st)
+
+    def frame(self) -> float:
+        """Seconds of oracle work for the next frame of the sampled layers
+        (input generation untimed)."""
+        sh, G = self.sh, self.sh.group
+        inputs = [self.src.layer_frame(0, l, self.n) for l in range(self.layers)]
+        t0 = time.perf_counter()
+        i = 0
+        for l in range(self.layers):
+            q, k, v = inputs[l]
+            for hk in range(sh.kv_heads):
+                self.orc.prefill_unit_frame(self.states[i], q[hk * G:(hk + 1) * G], k[hk], v[hk],
+                                            self.n, budget=sh.budget, omega=self.omega,
+                                            scale=self.scale, dtype=sh.dtype)
+                i += 1
+        self.n += 1
+        return time.perf_counter() - t0
 
 
-def cpu_baseline(sh, layers: int = 3) -> dict:
-    secs = _oracle_frame_sample(sh, layers)
-    per_frame = secs * sh.layers / layers
+def cpu_baseline(sh, frames: int = 8, layers: int = 1) -> dict:
+    """The oracle as it stands on 8 consecutive steady-state frames of one
+    layer (all its KV heads), scaled to every layer of the workload."""
+    smp = _OracleSample(sh, layers)
+    n0 = smp.n
+    secs = [smp.frame() for _ in range(frames)]
+    per_frame = sum(secs) / frames * sh.layers / layers
     return {"value": 1.0 / per_frame, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
-            "sample": f"fp64 NumPy oracle, {layers} of {sh.layers} layers "
-                      f"({layers * sh.kv_heads} of {sh.units} units) of one steady-state "
-                      f"frame (c=B={sh.budget}), {secs:.1f} s, scaled x{sh.layers}/{layers}"}
+            "kind": "oracle", "s_per_frame": per_frame,
+            "sample": f"fp64 NumPy oracle, {frames} consecutive steady-state frames "
+                      f"(n = {n0}..{n0 + frames - 1}, c = B = {sh.budget}) of {layers} of "
+                      f"{sh.layers} layers ({layers * sh.kv_heads} of {sh.units} units), "
+                      f"{sum(secs):.1f} s, scaled x{sh.layers}/{layers}"}
 
 
 def run_reference(args, sh):
@@ -190,24 +210,32 @@ def run_reference(args, sh):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     layers = 1
+    smp = _OracleSample(sh, layers)
     for _ in range(args.warmup):
-        _oracle_frame_sample(sh, layers)
-    times = [_oracle_frame_sample(sh, layers, seed=2 + i) for i in range(args.steps)]
-    tot = sum(times) * sh.layers / layers
-    value = args.steps / tot
+        smp.frame()
+    n0 = smp.n
+    times = [smp.frame() for _ in range(args.steps)]
+    timed = sum(times)
+    per_frame = timed / args.steps * sh.layers / layers     # all layers of one frame
+    value = 1.0 / per_frame
     cores = len(os.sched_getaffinity(0))
+    sample = (f"each step: the next steady-state frame (n = {n0}..{n0 + args.steps - 1}, c = B) "
+              f"of {layers} of {sh.layers} layers ({layers * sh.kv_heads} of {sh.units} units), "
+              f"the state continuing across steps; frames/s scaled x{sh.layers}/{layers}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * tot / args.steps, "higher_is_better": True,
+        # the measured time of what each step ran (one layer of one frame)
+        "ms_per_step": 1000.0 * timed / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": sh.name, "layers": sh.layers, "q_heads": sh.q_heads,
                    "kv_heads": sh.kv_heads, "head_dim": sh.head_dim, "T": sh.frame_tokens,
-                   "B": sh.budget, "step": "one steady-state frame, all layers (bounded "
-                                           "sample: 1 layer timed, scaled x28)"},
+                   "B": sh.budget, "step": f"one steady-state frame of {layers} layer(s)"},
+        "extrapolation": {"layers_timed_per_step": layers, "layers_per_frame": sh.layers,
+                          "value_scale": layers / sh.layers,
+                          "ms_per_frame_all_layers": 1000.0 * per_frame},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "one layer (2 units) of one steady-state frame per step, "
-                                   "scaled to all 28 layers"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -383,6 +411,19 @@ def run_gpu(args, sh):
     q_bytes = sh.streams * sh.layers * sh.q_heads * sh.frame_tokens * sh.head_dim * 2
     kv_bytes = sh.streams * sh.layers * sh.kv_heads * sh.frame_tokens * sh.head_dim * 2
     rope_bytes = 2 * q_bytes + 6 * kv_bytes
+    # select: the column partials read, scores and positions written, the
+    # live positions read, and the K/V rows moved by slot reuse (counted on
+    # the untimed video's last frame: its surviving frame rows)
+    T, B = sh.frame_tokens, sh.budget
+    m = min(B, (frames - 1) * T) + T
+    n_rt = -(-sh.group * T // 128)
+    moved = 0
+    for l in range(sh.layers):
+        for s_ in range(sh.streams):
+            _, _, p, c = h.compressed(s_, l)
+            moved += int((p[:, :c] >= (frames - 1) * T).sum().item())
+    sel_bytes = sh.units * (n_rt * m * 4 + 2 * m * 4 + min(B, (frames - 1) * T) * 4) \
+        + moved * 2 * 2 * sh.head_dim * 2
     kernels = {}
     for name, (kms, cnt) in prof.items():
         ent = {"launches_untimed_video": cnt, "ms_per_launch": kms / max(cnt, 1),
@@ -390,6 +431,12 @@ def run_gpu(args, sh):
         if name == "rope":
             ent["gbs"] = rope_bytes / (kms / max(cnt, 1) / 1000.0) / 1e9
             ent["algorithmic_bytes_per_launch"] = rope_bytes
+        if name == "select" and cnt:
+            ent["gbs"] = sel_bytes / (kms / cnt / 1000.0) / 1e9
+            ent["algorithmic_bytes_per_launch"] = sel_bytes
+            ent["rows_moved_last_frame"] = moved
+        if "gbs" in ent:
+            ent["frac_of_hbm"] = ent["gbs"] / peaks["hbm"]
         kernels[name] = ent
 
     if rank == 0:
@@ -457,11 +504,18 @@ def main():
     ap.add_argument("--policy", default="topb", choices=["topb", "window"],
                     help="selection: Top-B by score (the method) or the B most recent tokens "
                          "(the sliding-window baseline)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the workload's layer count (1 = one layer per launch, "
+                         "the shape of a model whose layers feed each other)")
     ap.add_argument("--budget", default="",
                     help="override B; 'full' = full self-attention (B covers every frame)")
     args = ap.parse_args()
     from synth import SHAPES
     sh = SHAPES[args.workload]
+    if args.layers:
+        sh = dataclasses.replace(sh, layers=args.layers,
+                                 name=f"{sh.name}_{args.layers}layer" if args.layers != sh.layers
+                                 else sh.name)
     if args.budget:
         frames = args.frames or sh.frames
         b = (frames + 1) * sh.frame_tokens if args.budget == "full" else int(args.budget)

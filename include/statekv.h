@@ -346,9 +346,11 @@ int statekv_profile_read(statekv_handle* h, int32_t kernel, double* total_ms,
  *   pool_k, pool_v [units][pool_rows][head_dim]     pool_rows >= compressed + frame_tokens
  *   o      [units][group * frame_tokens][head_dim]  written
  *   scores [units][compressed + frame_tokens] fp32  written
- *   status uint32[4] device status word (NULL: an internal one); a bounded
- *          device wait that gives up writes STATEKV_E_TIMEOUT into status[0]
- *          and leaves o and scores unspecified.
+ *   status uint32[4] device status word, required (4-byte aligned): the
+ *          call first zeroes it on cuda_stream; a bounded device wait that
+ *          gives up then writes STATEKV_E_TIMEOUT into status[0] (the wait
+ *          site into status[1]) and leaves o and scores unspecified.  Read
+ *          it once the stream has passed the call.
  * logit_scale = mscale^2 / sqrt(head_dim).  Returns STATEKV_E_CAPACITY when
  * units * ceil(group*frame_tokens / R) * round_up(pool_rows, 128) * 4 bytes
  * exceeds the 16 MiB scratch (R = 128 query rows per tile for bf16, 16 for

@@ -3,13 +3,17 @@
 Usage: python -m kv_cache_compression_frame_gb300.build_lib [--force] [-v]
 
 Each .cu file is compiled to an object in parallel, then linked into one
-shared library next to this file.  Objects are rebuilt when a source or a
-header is newer than them.
+shared library next to this file.  An object is rebuilt unless the SHA-256
+recorded beside it matches its source, every header and the compiler flags;
+the library is relinked unless its recorded hash matches its objects'.  A
+prebuilt object or library carried in from elsewhere, without the matching
+record, is therefore never reused.
 """
 
 from __future__ import annotations
 
 import argparse
+import hashlib
 import os
 import shutil
 import subprocess
@@ -37,44 +41,77 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _headers_mtime() -> float:
-    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    hs += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
-    return max(os.path.getmtime(h) for h in hs)
+def _sha(*parts: bytes) -> str:
+    h = hashlib.sha256()
+    for p in parts:
+        h.update(len(p).to_bytes(8, "little"))
+        h.update(p)
+    return h.hexdigest()
 
 
-def _compile(nvcc: str, src: str, force: bool, verbose: bool, extra: list[str]) -> str:
+def _read(path: str) -> bytes:
+    with open(path, "rb") as f:
+        return f.read()
+
+
+def _headers_digest() -> str:
+    hs = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
+    hs += sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE))
+    return _sha(*[os.path.basename(h).encode() + b"\0" + _read(h) for h in hs])
+
+
+def _stamp_ok(target: str, digest: str) -> bool:
+    stamp = target + ".sha"
+    return (os.path.exists(target) and os.path.exists(stamp)
+            and _read(stamp).decode().strip() == digest)
+
+
+def _write_stamp(target: str, digest: str) -> None:
+    with open(target + ".sha", "w") as f:
+        f.write(digest + "\n")
+
+
+def _compile(nvcc: str, src: str, force: bool, verbose: bool, extra: list[str],
+             headers: str) -> tuple[str, str]:
     obj = os.path.join(BUILD, src.replace(".cu", ".o"))
     path = os.path.join(CSRC, src)
-    if (not force and os.path.exists(obj)
-            and os.path.getmtime(obj) >= max(os.path.getmtime(path), _headers_mtime())):
-        return obj
     cmd = [nvcc, *CFLAGS, *extra, "-c", path, "-o", obj]
+    digest = _sha(_read(path), headers.encode(), " ".join([*CFLAGS, *extra]).encode())
+    if not force and _stamp_ok(obj, digest):
+        return obj, digest
     if verbose:
         print(" ".join(cmd), flush=True)
+    if os.path.exists(obj + ".sha"):
+        os.remove(obj + ".sha")
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
     if verbose and (r.stdout or r.stderr):
         print(r.stdout + r.stderr, flush=True)
-    return obj
+    _write_stamp(obj, digest)
+    return obj, digest
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    headers = _headers_digest()
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(nvcc, s, force or ptxas_info, verbose, extra),
-                           SOURCES))
-    if (force or not os.path.exists(LIB)
-            or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)):
+        built = list(ex.map(lambda s: _compile(nvcc, s, force or ptxas_info, verbose, extra,
+                                               headers), SOURCES))
+    objs = [o for o, _ in built]
+    digest = _sha(*[d.encode() for _, d in built], " ".join(ARCH).encode())
+    if force or not _stamp_ok(LIB, digest):
+        if os.path.exists(LIB + ".sha"):
+            os.remove(LIB + ".sha")
         tmp = LIB + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+        _write_stamp(LIB, digest)
     return LIB
 
 

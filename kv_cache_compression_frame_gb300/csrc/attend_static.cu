@@ -33,17 +33,15 @@ constexpr size_t kStaticScratchFloats = kStaticScratchBytes / sizeof(float);
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_colsum_scratch[kStaticScratchFloats];
-static __device__ __align__(256) uint32_t g_status_scratch[statekv::kErrWords];
 
 struct StaticScratch {
     float* colsum = nullptr;
-    uint32_t* status = nullptr;
     bool ready = false;
 };
 StaticScratch g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device addresses of the static arrays for the current device.
+// Device address of the static scratch for the current device.
 int scratch_for_device(int dev, StaticScratch** out) {
     if (dev < 0 || dev >= kMaxDevices) return STATEKV_E_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
@@ -52,8 +50,6 @@ int scratch_for_device(int dev, StaticScratch** out) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_colsum_scratch) != cudaSuccess) return STATEKV_E_CUDA;
         s.colsum = static_cast<float*>(p);
-        if (cudaGetSymbolAddress(&p, g_status_scratch) != cudaSuccess) return STATEKV_E_CUDA;
-        s.status = static_cast<uint32_t*>(p);
         s.ready = true;
     }
     *out = &s;
@@ -82,7 +78,7 @@ extern "C" int statekv_attend_scores_static(
     using namespace statekv;
     for (const void* p : {q_rot, pool_k, pool_v, static_cast<const void*>(o)})
         if (!p || reinterpret_cast<uintptr_t>(p) % 16) return STATEKV_E_INVALID_ARG;
-    if (!scores) return STATEKV_E_INVALID_ARG;
+    if (!scores || !status || reinterpret_cast<uintptr_t>(status) % 4) return STATEKV_E_INVALID_ARG;
     if (units < 1 || group < 1 || frame_tokens < 1 || compressed < 0 ||
         pool_rows < compressed + frame_tokens || !(logit_scale > 0.0))
         return STATEKV_E_INVALID_ARG;
@@ -102,11 +98,15 @@ extern "C" int statekv_attend_scores_static(
     int r = scratch_for_device(dev, &sc);
     if (r != STATEKV_OK) return r;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    // the status word reports this call only: a failure keeps the first
+    // error it finds in a zero word, so a stale one would hide it
+    if (cudaMemsetAsync(status, 0, kErrWords * sizeof(uint32_t), st) != cudaSuccess)
+        return STATEKV_E_CUDA;
 
     AttnArgs a{};
     a.q_rot = q_rot; a.pool_k = pool_k; a.pool_v = pool_v; a.o = o;
     a.colsum = sc->colsum;
-    a.err = status ? status : sc->status;
+    a.err = status;
     a.U = units; a.GT = (int32_t)GT; a.T = frame_tokens; a.d = head_dim;
     a.slots = pool_rows; a.c = compressed; a.m_pad = (int32_t)m_pad;
     a.n_row_tiles = (int32_t)n_row_tiles;

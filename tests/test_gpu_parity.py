@@ -15,7 +15,7 @@ import torch
 import oracle.statekv_oracle as orc
 from synth import SHAPES, FrameSource, WorkloadShape
 from parity import (O_TOL, check_rope, check_scores, check_selection, f64,
-                    raw_equal, row_rel_err)
+                    raw_equal, record_step, row_rel_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +64,21 @@ class Stepper:
         o = self.h.prefill_frame(q, k, v)
         self.h.check_device_status()
         return o
+
+    def advance(self, n_to, ring=4):
+        """Run frames up to (not including) n_to quickly: frame n takes the
+        inputs of frame n % ring (generated once).  The frames checked later
+        with step() come from the source itself; the checks are
+        teacher-forced on the GPU's state, so only the shape of the history
+        matters here, not its values."""
+        if not hasattr(self, "_ring"):
+            self._ring = [self.tensors(i)[1] for i in range(max(1, min(ring, n_to)))]
+        n = self.h.frame_index
+        while n < n_to:
+            q, k, v = self._ring[n % len(self._ring)]
+            self.h.prefill_frame(q, k, v)
+            n += 1
+        self.h.check_device_status()
 
     def step(self, n, units=None):
         sh, h = self.sh, self.h
@@ -122,6 +137,7 @@ class Stepper:
             assert raw_equal(nk[hk, :ncnt].cpu(), pool_k_raw[idx]), f"C K gather {what}"
             assert raw_equal(nv[hk, :ncnt].cpu(), pool_v_raw[idx]), f"C V gather {what}"
         self.stats.append((n, worst))
+        record_step(self.sh.name, n, len(units), worst)
         return worst
 
 
@@ -183,6 +199,49 @@ def test_full_size_steady_state_sampled(name, layers):
         st.run(n)
     units = [(0, l, hk) for l in layers for hk in range(sh.kv_heads)]
     st.step(16, units=units)
+
+
+@pytest.mark.parametrize("name,layers", [("internvl3_2b_stack", (0, 27)),
+                                         ("qwen3vl_2b_stack", (0, 27))])
+def test_full_size_last_frame_sampled(name, layers):
+    """The last frame of a 512-frame video (n = 511): positions reach
+    130,816..131,071 (the fp64 angle reduction and the alpha = 4 YaRN
+    frequencies carry all of RoPE's accuracy there) and the step appends
+    the last rows the detailed state can hold (n = max_frames - 1)."""
+    sh = SHAPES[name]
+    st = Stepper(sh)
+    st.advance(sh.frames - 1)
+    units = [(0, l, hk) for l in layers for hk in range(sh.kv_heads)]
+    st.step(sh.frames - 1, units=units)
+    _, _, dcnt = st.h.detailed(0, layers[-1])
+    assert dcnt == sh.frames * sh.frame_tokens
+
+
+def test_internvl3_2b_budget_16384_steady_state():
+    """The largest budget of the page's budget ablation (B = 16384): a pool of
+    16,640 candidates per unit (a wider radix cut and key buffer in the
+    selection, 130 key tiles per query tile), checked on the first two
+    frames with a full state."""
+    sh = SHAPES["internvl3_2b_stack"].with_(name="internvl3_2b_B16384", budget=16384, frames=80)
+    st = Stepper(sh)
+    n_full = sh.budget // sh.frame_tokens
+    st.advance(n_full)
+    units = [(0, l, hk) for l in (0, 27) for hk in range(sh.kv_heads)]
+    for n in (n_full, n_full + 1):
+        st.step(n, units=units)
+
+
+@pytest.mark.parametrize("name,n", [("serving_T64_B1024", 17), ("serving_T64_B4096", 65),
+                                    ("serving_T256_B1024", 5)])
+def test_serving_shape_steady_state_sampled(name, n):
+    """The batched-serving configuration: 16 independent streams x 4 layers x
+    8 KV heads stepped together (512 units; at T = 64 one 128-row query tile
+    per unit), checked after the state filled, on sampled streams."""
+    sh = SHAPES[name]
+    st = Stepper(sh)
+    st.advance(n)
+    units = [(s, l, hk) for s in (0, 7, 15) for l in (0, 3) for hk in range(sh.kv_heads)]
+    st.step(n, units=units)
 
 
 def test_teacher_forced_from_oracle_state():
