@@ -108,14 +108,19 @@ typedef struct statekv_handle statekv_handle;   /* opaque */
  * Limits: G*T <= 65536 query rows per unit; B + T <= 24576 unless
  * B >= max_frames*T (no eviction: then only memory bounds the pool);
  * positions must fit in int32.
- * The bf16 attention runs one CTA per 128-row query tile; the tiles of the
- * last, partial wave (when it
- * fills at most half the SMs after at least one full wave) are each
- * computed by two CTAs of a cluster, one half of the key tiles each, which
- * exchange their row log-sum-exps and output halves through distributed
- * shared memory; results agree with whole tiles up to rounding.
- * STATEKV_ATTN_SPLIT, read at every prefill launch, overrides which tiles
- * do so: 0 = none, all = every tile, n = the last n tiles.
+ * The bf16 attention runs one CTA per 128-row query tile.  Some tiles are
+ * split over their keys among the CTAs of a thread-block cluster, which
+ * exchange their row log-sum-exps and partial outputs through distributed
+ * shared memory (results agree with whole tiles up to rounding, and are
+ * deterministic): with at least one full wave of tiles (one per SM), the
+ * tiles of the last, partial wave when it fills at most half the SMs, as
+ * pairs; with fewer tiles than SMs (for example one layer per call), every
+ * tile, over 2..8 CTAs chosen from how many such clusters the device holds
+ * at once.  The selection likewise spreads each unit over a cluster of up to
+ * 8 CTAs when the units are few.  Test overrides, read at every prefill
+ * launch: STATEKV_ATTN_SPLIT (0 = no split, all = every tile, n = the last n
+ * tiles) with STATEKV_ATTN_SPLIT_WAYS (2..8, default 2), and
+ * STATEKV_SELECT_CLUSTER (1, 2, 4 or 8 CTAs per unit).
  */
 typedef struct statekv_config {
     int32_t num_streams;

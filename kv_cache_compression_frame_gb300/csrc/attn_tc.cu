@@ -55,6 +55,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include <type_traits>
 
@@ -62,6 +63,8 @@
 
 namespace statekv {
 namespace {
+
+constexpr int L_KSMAX = 8;                              // largest key split (cluster size)
 
 template <int D>
 struct TcLayout {
@@ -78,8 +81,9 @@ struct TcLayout {
     static constexpr int OFF_COL = OFF_V + VS * TILE;   // float [NCOL][4 quarters][128]
     static constexpr int OFF_STAT = OFF_COL + NCOL * 4 * 128 * 4;   // float2 [16 threads][128 rows]
     static constexpr int OFF_LSE = OFF_STAT + 16 * 128 * 8;         // float [128 rows]
-    static constexpr int OFF_XLSE = OFF_LSE + 128 * 4;  // float [128 rows]: the other key half's lse
-    static constexpr int OFF_BAR = OFF_XLSE + 128 * 4;
+    static constexpr int KSMAX = L_KSMAX;
+    static constexpr int OFF_XLSE = OFF_LSE + 128 * 4;  // float [KSMAX][128 rows]: the split's lse partials
+    static constexpr int OFF_BAR = OFF_XLSE + KSMAX * 128 * 4;
     static constexpr int B_Q = 0;                       // Q in TMEM (all softmax warps)
     static constexpr int B_K_FULL = 1;
     static constexpr int B_K_EMPTY = B_K_FULL + KS;
@@ -94,10 +98,10 @@ struct TcLayout {
     static constexpr int B_STAT = B_DRAIN + 2;          // row statistics of every softmax thread stored
     static constexpr int B_LSE = B_STAT + 1;            // lse of every row stored
     static constexpr int B_S1_DONE = B_LSE + 1;         // the PV warp issued its sweep-1 S tiles
-    // split query tiles (two CTAs of a cluster, one key half each):
-    static constexpr int B_XLSE = B_S1_DONE + 1;        // the other half's lse partials arrived
-    static constexpr int B_XREADY = B_XLSE + 1;         // the other half's K stages may take our O
-    static constexpr int B_XO = B_XREADY + 1;           // the other half's O columns arrived
+    // split query tiles (the ks CTAs of a cluster, one key range each):
+    static constexpr int B_XLSE = B_S1_DONE + 1;        // every other CTA's lse partials arrived
+    static constexpr int B_XREADY = B_XLSE + 1;         // every other CTA's K stages may take our O
+    static constexpr int B_XO = B_XREADY + 1;           // the O columns this CTA owns arrived
     static constexpr int NBAR = B_XO + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
@@ -105,6 +109,16 @@ struct TcLayout {
     static constexpr uint32_t TM_O = 256, TM_P = 384, TM_Q = 448;
     static constexpr int THREADS = 96 + 32 * SW;
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+    // a split tile's owner receives ks partial O blocks of bw columns x 128
+    // rows (fp32) in its K stages
+    static constexpr bool split_fits() {
+        for (int ks = 2; ks <= KSMAX; ++ks) {
+            const int bw = 8 * ((D + 8 * ks - 1) / (8 * ks));
+            if (ks * bw * 128 * 4 > KS * TILE) return false;
+        }
+        return true;
+    }
+    static_assert(split_fits(), "split O exchange fits in the K stages");
 };
 
 // Key range of one 128-row query tile: tiles [0, nt) hold a key visible to
@@ -124,18 +138,27 @@ __device__ __forceinline__ TileRange tile_range(int row0, int GT, int T, int c) 
     return r;
 }
 
-// SPLIT: the grid is clusters of two CTAs.  The first split_item0 query
-// tiles run whole, two per cluster (the CTAs do not interact); each later
-// tile is shared by the two CTAs of a cluster ("coop"), each taking one half
-// of its key tiles: they exchange the per-row lse partials after sweep 1 and
-// add each other's O columns at the end (through distributed shared memory).
-// The last, partial wave runs this way, so its tiles take about 60 % as long
-// on twice as many SMs, and start as soon as SMs free up in the wave before.
-template <int D, bool SPLIT>
+// SPLIT: the grid is clusters of ks = a.split_ks CTAs.  The first
+// split_item0 query tiles run whole, ks per cluster (the CTAs do not
+// interact); each later tile is shared by the ks CTAs of a cluster ("coop"),
+// CTA r taking key tiles [r*nt/ks, (r+1)*nt/ks): after sweep 1 every CTA
+// sends its per-row lse partials to the others and all combine them in rank
+// order (the same bits everywhere); at the end CTA r owns O columns
+// [r*bw, (r+1)*bw) (bw a multiple of 8), receives the other CTAs' partial O
+// of them through distributed shared memory and adds the ks partials in
+// rank order.  Two uses: the last, partial wave of a launch of several
+// waves runs as pairs (its tiles take about 60 % as long on twice as many
+// SMs, and start as soon as SMs free up in the wave before), and a launch
+// with fewer tiles than SMs (one layer at a time) spreads every tile's keys
+// over ks CTAs.
+// KSC: the split width, 1 = no split tiles, 2 = pairs (the tail of a launch
+// of several waves), 0 = a.split_ks CTAs (a launch of fewer tiles than SMs).
+template <int D, int KSC>
 __global__ void __launch_bounds__(TcLayout<D>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, AttnArgs a) {
     using L = TcLayout<D>;
+    constexpr bool SPLIT = KSC != 1;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -143,16 +166,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rt = a.n_row_tiles;
-    const int pair = (int)(blockIdx.x >> 1);
-    const bool coop = SPLIT && 2 * pair >= a.split_item0;
-    const int half = coop ? (int)ptx::cluster_ctarank() : 0;
-    const int item = coop ? a.split_item0 + (pair - a.split_item0 / 2) : (int)blockIdx.x;
+    const int ks = KSC > 0 ? KSC : a.split_ks;
+    const int cl = (int)blockIdx.x / ks;                 // cluster
+    const bool coop = SPLIT && cl * ks >= a.split_item0;
+    const int rank = coop ? (int)ptx::cluster_ctarank() : 0;
+    const int item = coop ? a.split_item0 + (cl - a.split_item0 / ks) : (int)blockIdx.x;
+    // O columns [rank*bw, (rank+1)*bw) are this CTA's to output in a split tile
+    const int bw = 8 * ((D + 8 * ks - 1) / (8 * ks));
     const int u = item / n_rt;
     const int mt = item - u * n_rt;
     const TileRange me = tile_range(mt * 128, a.GT, a.T, a.c);
     // this CTA's key tiles: [t0, t0 + nt_mine) of the tile's [0, me.nt)
-    const int t0 = coop && half ? me.nt / 2 : 0;
-    const int nt_mine = coop ? (half ? me.nt - me.nt / 2 : me.nt / 2) : me.nt;
+    const int t0 = coop ? rank * me.nt / ks : 0;
+    const int nt_mine = coop ? (rank + 1) * me.nt / ks - t0 : me.nt;
 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::OFF_MISC);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + L::OFF_MISC + 4);
@@ -182,9 +208,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::mbar_init(sy.bar(L::B_STAT), L::SW);
         ptx::mbar_init(sy.bar(L::B_LSE), 4);
         ptx::mbar_init(sy.bar(L::B_S1_DONE), 1);
-        ptx::mbar_init(sy.bar(L::B_XLSE), 128);                    // 4 warps x 32 lanes
-        ptx::mbar_init(sy.bar(L::B_XREADY), L::SW);
-        ptx::mbar_init(sy.bar(L::B_XO), (D / 64) * 128);          // the peer's senders, per lane
+        // split tiles: 128 rows of lse partials from each other CTA; its 16
+        // softmax warps' "K stages consumed"; and one arrive per sending
+        // lane (4 quarters x 32 lanes of every 32-column chunk that overlaps
+        // this CTA's columns) from each other CTA
+        const int lo = rank * bw, hi = min(D, lo + bw);
+        const int nwin = lo < hi ? (hi - 1) / 32 - lo / 32 + 1 : 0;
+        ptx::mbar_init(sy.bar(L::B_XLSE), (uint32_t)max(1, 128 * (ks - 1)));
+        ptx::mbar_init(sy.bar(L::B_XREADY), (uint32_t)max(1, L::SW * (ks - 1)));
+        ptx::mbar_init(sy.bar(L::B_XO), (uint32_t)max(1, 128 * nwin * (ks - 1)));
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -194,8 +226,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // a split tile's other half writes into this CTA's shared memory and
-    // arrives on its barriers: all of them must be initialised first
+    // a split tile's other CTAs write into this CTA's shared memory and
+    // arrive on its barriers: all of them must be initialised first
     if (coop) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
@@ -557,18 +589,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
             float lse = (me.row0 + row < a.GT && l > 0.f) ? fmaf(m, sc, log2f(l)) : INFINITY;
             if (SPLIT && coop) {
-                // the row's lse over this CTA's key half (-inf: no key), sent
-                // to the other half; both combine the two partials
+                // the row's lse over this CTA's key range (-inf: no key),
+                // sent to every other CTA of the split; all combine the ks
+                // partials in rank order, so every CTA gets the same bits
                 const float part = l > 0.f ? fmaf(m, sc, log2f(l)) : -INFINITY;
-                const uint32_t peer = (uint32_t)(half ^ 1);
-                ptx::st_cluster_f32(ptx::cluster_map(sbase + L::OFF_XLSE + 4u * row, peer), part);
-                ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XLSE), peer));
+                const uint32_t slot = sbase + L::OFF_XLSE + 4u * (uint32_t)(rank * 128 + row);
+                for (int j = 0; j < ks; ++j) {
+                    if (j == rank) continue;
+                    ptx::st_cluster_f32(ptx::cluster_map(slot, (uint32_t)j), part);
+                    ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XLSE), (uint32_t)j));
+                }
                 if (!sy.wait_cluster(L::B_XLSE, 0, kSiteCol)) ok = false;
-                const float other = reinterpret_cast<const float*>(base + L::OFF_XLSE)[row];
-                const float mx = fmaxf(part, other);
-                lse = (me.row0 + row < a.GT && mx != -INFINITY)
-                          ? mx + log2f(exp2f(part - mx) + exp2f(other - mx))
-                          : INFINITY;
+                const float* xl = reinterpret_cast<const float*>(base + L::OFF_XLSE);
+                float mx = -INFINITY;
+                for (int j = 0; j < ks; ++j) mx = fmaxf(mx, j == rank ? part : xl[j * 128 + row]);
+                float sum = 0.f;
+                if (mx != -INFINITY)
+                    for (int j = 0; j < ks; ++j)
+                        sum += exp2f((j == rank ? part : xl[j * 128 + row]) - mx);
+                lse = (me.row0 + row < a.GT && mx != -INFINITY) ? mx + log2f(sum) : INFINITY;
             }
             lsebuf[row] = lse;
             __syncwarp();
@@ -659,24 +698,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_P_FULL + ph));
         }
         if (SPLIT && coop) {
-            // this CTA's key tiles are consumed: the other half may put its
-            // O columns into our K stages
+            // this CTA's key tiles are consumed: the others may put their O
+            // columns into our K stages
             __syncwarp();
             if (lane == 0)
-                ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XREADY), (uint32_t)(half ^ 1)));
+                for (int j = 0; j < ks; ++j)
+                    if (j != rank)
+                        ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XREADY), (uint32_t)j));
         }
-        if (me.nt > 0 && (!coop || half == 1))         // the half holding the last tiles
+        if (me.nt > 0 && (!coop || rank == ks - 1))    // the CTA holding the last tiles
             for (int kk = me.nt * L::BN + sw * 32 + lane; kk < a.m_pad; kk += 32 * L::SW)
                 colsum[kk] = 0.f;
 
         // ---- output rows: quarter q4, 32 columns per warp
         if (SPLIT && coop) {
-            // each half outputs D/2 columns: it adds the other half's partial
-            // O of them (stored column-major into its K stage 0, so a warp's
-            // 32 lanes = 32 rows write consecutive words) to its own
+            // CTA r outputs columns [r*bw, (r+1)*bw): the others store their
+            // partial O of them column-major into its K stages (slot of
+            // sender j at [j*bw][128], so a warp's 32 lanes = 32 rows write
+            // consecutive words) and it adds the ks partials in rank order
             if (cq < D / 32) {
-                const int owner = (cq * 2) / (D / 32);
-                const int c0 = 32 * cq - owner * (D / 2);
+                const int c0 = 32 * cq;
                 const int row = q4 * 32 + lane;
                 float v[32];
                 bool have = false;
@@ -693,28 +734,46 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.f;   // no key tiles: no mass
                 }
-                const uint32_t peer = (uint32_t)(half ^ 1);
-                if (owner != half) {
+                // owners of this warp's 32 columns (bw is a multiple of 8)
+                const int o_lo = c0 / bw, o_hi = min((c0 + 31) / bw, ks - 1);
+                if (o_lo != rank || o_hi != rank) {
                     if (sy.wait_cluster(L::B_XREADY, 0, kSiteCol)) {
-                        const uint32_t dst = ptx::cluster_map(sK, peer);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            ptx::st_cluster_f32(dst + 4u * (uint32_t)((c0 + j) * 128 + row), v[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int o = (c0 + j) / bw;
+                            if (o != rank) {
+                                const uint32_t col = (uint32_t)(rank * bw + (c0 + j - o * bw));
+                                ptx::st_cluster_f32(ptx::cluster_map(sK + 4u * (col * 128 + row),
+                                                                     (uint32_t)o), v[j]);
+                            }
+                        }
                     }
-                    ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XO), peer));
-                } else if (sy.wait_cluster(L::B_XO, 0, kSiteCol) && me.row0 + row < a.GT) {
+                    for (int o = o_lo; o <= o_hi; ++o)
+                        if (o != rank)
+                            ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XO), (uint32_t)o));
+                }
+                const int lo = max(c0, rank * bw), hi = min(c0 + 32, (rank + 1) * bw);
+                if (lo < hi && sy.wait_cluster(L::B_XO, 0, kSiteCol) && me.row0 + row < a.GT) {
                     const float* xo = reinterpret_cast<const float*>(base + L::OFF_K);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] += xo[(c0 + j) * 128 + row];
                     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                         ((int64_t)u * a.GT + me.row0 + row) * D + 32 * cq;
-                    uint32_t wv[16];
+                                         ((int64_t)u * a.GT + me.row0 + row) * D + c0;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) wv[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
-                    uint4* dst = reinterpret_cast<uint4*>(out);
+                    for (int g = 0; g < 4; ++g) {
+                        if (c0 + 8 * g < lo || c0 + 8 * g >= hi) continue;
+                        uint32_t wv[4];
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
+                        for (int e = 0; e < 8; e += 2) {
+                            const int j = 8 * g + e;
+                            const int col = c0 + j - rank * bw;      // within this CTA's columns
+                            float s0 = 0.f, s1 = 0.f;
+                            for (int r = 0; r < ks; ++r) {
+                                s0 += r == rank ? v[j] : xo[(r * bw + col) * 128 + row];
+                                s1 += r == rank ? v[j + 1] : xo[(r * bw + col + 1) * 128 + row];
+                            }
+                            wv[e / 2] = ptx::pack_bf16x2(s0, s1);
+                        }
+                        reinterpret_cast<uint4*>(out)[g] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
                 }
             }
         } else if (me.nt > 0 && ok && cq < D / 32 && sy.wait(L::B_O_FULL, 0, kSiteOFull)) {
@@ -749,58 +808,130 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
 }
 
-template <int D, bool SPLIT>
-cudaError_t launch_grid(const AttnArgs& a, const TcMaps& m, cudaStream_t st, int grid) {
+template <int D>
+cudaLaunchConfig_t grid_config(cudaStream_t st, int grid, int ks, cudaLaunchAttribute (&attr)[2]) {
     using L = TcLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, SPLIT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(L::THREADS);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = SPLIT ? 2 : 1;
+    attr[0].val.clusterDim.x = (unsigned)ks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, SPLIT>, m.k, m.v, a);
+    return cfg;
 }
 
-// Query tiles run as a key-split pair: the tiles of the last, partial wave
-// (one CTA per SM, a.resident SMs), when it fills at most half the SMs after
-// at least one full wave.  STATEKV_ATTN_SPLIT overrides: 0 = none, all =
-// every tile, n = the last n tiles.
-int split_tiles(int items, int resident) {
+template <int D, int KSC>
+cudaError_t launch_grid(const AttnArgs& a, const TcMaps& m, cudaStream_t st, int grid) {
+    using L = TcLayout<D>;
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, KSC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = grid_config<D>(st, grid, a.split_ks, attr);
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, KSC>, m.k, m.v, a);
+}
+
+// Clusters of ks split CTAs that one wave holds on this device (0 when the
+// query fails), cached per (device, D, ks).
+template <int D>
+int clusters_per_wave(int ks) {
+    static std::mutex mu;
+    static int cache[64][L_KSMAX + 1];
+    static bool init = false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!init) {
+        for (auto& row : cache)
+            for (int& x : row) x = -1;
+        init = true;
+    }
+    int& c = cache[dev][ks];
+    if (c < 0) {
+        c = 0;
+        if (cudaFuncSetAttribute(attn_tc_kernel<D, 0>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcLayout<D>::SMEM) == cudaSuccess) {
+            cudaLaunchAttribute attr[2];
+            const cudaLaunchConfig_t cfg = grid_config<D>(nullptr, ks, ks, attr);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<D, 0>, &cfg) == cudaSuccess)
+                c = n;
+        }
+        cudaGetLastError();
+    }
+    return c;
+}
+
+// Which query tiles run split over their keys, and over how many CTAs.
+//  * At least one full wave (one CTA per SM, a.resident SMs): the tiles of
+//    the last, partial wave, when it fills at most half the SMs, as pairs.
+//  * Fewer tiles than SMs (e.g. one layer per launch): every tile, over the
+//    ks in 1..8 with the least estimated time, waves(ks) * (P + nt / ks):
+//    nt key tiles per query tile (at most), P ~ 4 key tiles' worth of
+//    per-CTA set-up, exchange and output, waves from the clusters of ks CTAs
+//    the device holds at once (a cluster needs ks free SMs of one GPC).
+// STATEKV_ATTN_SPLIT overrides which tiles: 0 = none, all = every tile, n =
+// the last n; STATEKV_ATTN_SPLIT_WAYS (2..8, default 2) the CTAs per tile.
+struct SplitPlan {
+    int split;      // tiles split (the last ones)
+    int ks;         // CTAs per split tile
+};
+
+template <int D>
+SplitPlan plan_split(const AttnArgs& a, int items) {
     const char* env = std::getenv("STATEKV_ATTN_SPLIT");
     if (env && *env) {
-        if (std::strcmp(env, "all") == 0) return items;
+        int ks = 2;
+        if (const char* w = std::getenv("STATEKV_ATTN_SPLIT_WAYS"))
+            ks = std::max(2, std::min(L_KSMAX, std::atoi(w)));
+        if (std::strcmp(env, "all") == 0) return {items, ks};
         const long n = std::strtol(env, nullptr, 10);
-        return (int)std::max(0L, std::min((long)items, n));
+        return {(int)std::max(0L, std::min((long)items, n)), ks};
     }
-    if (resident <= 0) return 0;
-    const int full = items / resident * resident, tail = items - full;
-    return (full > 0 && tail > 0 && 2 * tail <= resident) ? tail : 0;
+    if (a.resident <= 0) return {0, 1};
+    if (items >= a.resident) {
+        const int full = items / a.resident * a.resident, tail = items - full;
+        return {(tail > 0 && 2 * tail <= a.resident) ? tail : 0, 2};
+    }
+    const double nt = (double)((a.c + a.T + 127) / 128);
+    constexpr double P = 4.0;
+    int best = 1;
+    double best_cost = P + nt;                   // unsplit: one wave
+    for (int ks = 2; ks <= L_KSMAX; ++ks) {
+        const int per_wave = clusters_per_wave<D>(ks);
+        if (per_wave <= 0) continue;
+        const double waves = (double)((items + per_wave - 1) / per_wave);
+        const double cost = waves * (P + nt / ks);
+        if (cost < best_cost) { best_cost = cost; best = ks; }
+    }
+    return best > 1 ? SplitPlan{items, best} : SplitPlan{0, 1};
 }
 
 template <int D>
 cudaError_t launch_tc(const AttnArgs& a_in, const TcMaps& m, cudaStream_t st) {
     const int items = a_in.U * a_in.n_row_tiles;
     AttnArgs a = a_in;
-    int split = split_tiles(items, a.resident);
-    if (split == 0) {
+    SplitPlan p = plan_split<D>(a, items);
+    if (p.split == 0) {
         a.split_item0 = items;
-        return launch_grid<D, false>(a, m, st, items);
+        a.split_ks = 1;
+        return launch_grid<D, 1>(a, m, st, items);
     }
-    // whole tiles go two per cluster: an even count
-    if ((items - split) & 1) ++split;
+    // whole tiles go ks per cluster: a multiple of ks of them
+    const int ks = p.ks;
+    int split = p.split + (items - p.split) % ks;
     a.split_item0 = items - split;
-    return launch_grid<D, true>(a, m, st, a.split_item0 + 2 * split);
+    a.split_ks = ks;
+    const int grid = a.split_item0 + ks * split;
+    return ks == 2 ? launch_grid<D, 2>(a, m, st, grid) : launch_grid<D, 0>(a, m, st, grid);
 }
 
 }  // namespace

@@ -26,6 +26,17 @@
 // 512-thread ones: eight warps per sub-partition): per-thread work is kept to
 // a few instructions per key (32-bit keys, warp ballots for the slot-ordered
 // lists), since each one costs eight issue slots.
+// With few units (one layer per launch: 2-8 units on 152 SMs) a unit is a
+// cluster of C CTAs: CTA r finishes the scores of candidates
+// [r*m/C, (r+1)*m/C) and stores their keys into every CTA's shared memory
+// (distributed shared memory); after one cluster barrier each CTA holds all
+// m keys and runs steps 3-4's cut and lists itself (the same inputs, so the
+// same result everywhere), then moves its share of the rows.  Step 1, which
+// reads all the partials, and the row moves are spread over C SMs.
+#include <cstdlib>
+#include <mutex>
+#include <vector>
+
 #include "statekv_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -154,6 +165,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     int32_t* movers = holes + min(a.B, a.T);
     __shared__ uint32_t gtot[32], rout[3];
     __shared__ uint32_t s_and[kMaxWarps], s_or[kMaxWarps];
+    __shared__ uint32_t c_and[8], c_or[8];          // per CTA of the unit's cluster
     __shared__ uint32_t wtot[2][kMaxWarps];
     __shared__ uint32_t s_pairs;
 
@@ -162,13 +174,20 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     // finished.  Then the next frame's RoPE kernel may start (it rewrites
     // Q', which the attention kernel read, and waits for this grid before
     // it writes the pool rows read here)
+    // a cluster's CTAs store keys into each other's shared memory: each
+    // first has to know the others have started (arrive here, wait below)
+    const bool cl_bar = a.cluster > 1 && a.c + a.T > a.B;
+    if (cl_bar) ptx::cluster_arrive_relaxed();
     ptx::dep_wait();
     ptx::dep_trigger();
-    const int u = blockIdx.x;
+    const int C = a.cluster;
+    const int rank = C > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int u = (int)blockIdx.x / C;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int c = a.c, T = a.T, B = a.B;
     const int m = c + T;
+    const int j_lo = rank * m / C, j_hi = (rank + 1) * m / C;   // this CTA's candidates
     int32_t* pos = a.pos + (int64_t)u * a.slots;
     if (m > B) {                                // the histograms start at zero
         uint4* hv = reinterpret_cast<uint4*>(hist);
@@ -186,7 +205,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     constexpr int KU = 2, TU = 12;
     const int n_rt = a.n_row_tiles;
     uint32_t k_and = ~0u, k_or = 0u;
-    for (int j0 = tid; j0 < m; j0 += KU * NT) {
+    const uint32_t vals_s = ptx::smem_u32(vals);
+    if (cl_bar) ptx::cluster_wait();
+    for (int j0 = j_lo + tid; j0 < j_hi; j0 += KU * NT) {
         float sv[KU];
         int32_t pv[KU];
 #pragma unroll
@@ -194,7 +215,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
             const int j = j0 + q * NT;
             sv[q] = 0.f;
             pv[q] = 0;
-            if (j < m) pv[q] = j < c ? pos[j] : a.pos_base + (j - c);
+            if (j < j_hi) pv[q] = j < c ? pos[j] : a.pos_base + (j - c);
         }
         for (int t0 = 0; t0 < n_rt; t0 += TU) {
             float part[KU][TU];
@@ -203,7 +224,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
                 const int j = j0 + q * NT;
 #pragma unroll
                 for (int tt = 0; tt < TU; ++tt)
-                    part[q][tt] = (j < m && t0 + tt < n_rt)
+                    part[q][tt] = (j < j_hi && t0 + tt < n_rt)
                                       ? __ldcg(cs + (int64_t)(t0 + tt) * a.m_pad + j) : 0.f;
             }
             // tile order: s_j has the same bits whatever the tiling above
@@ -216,7 +237,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
 #pragma unroll
         for (int q = 0; q < KU; ++q) {
             const int j = j0 + q * NT;
-            if (j < m) {
+            if (j < j_hi) {
                 sv[q] *= a.inv_rows;
                 scores[j] = sv[q];
                 spos[j] = pv[q];
@@ -230,9 +251,18 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
         }
     }
     if (m <= B) {                               // state not full: keep all
-        for (int j = c + tid; j < m; j += NT) pos[j] = a.pos_base + (j - c);
+        for (int j = max(c, j_lo) + tid; j < j_hi; j += NT) pos[j] = a.pos_base + (j - c);
         return;
     }
+    // this CTA's keys to the other CTAs of the unit (each thread sends the
+    // keys it wrote itself)
+    if (C > 1)
+        for (int j = j_lo + tid; j < j_hi; j += NT) {
+            const uint32_t k = vals[j];
+            for (int r = 0; r < C; ++r)
+                if (r != rank)
+                    ptx::st_cluster_u32(ptx::cluster_map(vals_s + 4u * (uint32_t)j, (uint32_t)r), k);
+        }
 
     // ---- 3. the cut of the E smallest keys
     {
@@ -241,11 +271,24 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
         if (lane == 0) { s_and[warp] = wa; s_or[warp] = wo; }
     }
     __syncthreads();
+    uint32_t all_and = __reduce_and_sync(0xffffffffu, lane < NW ? s_and[lane] : ~0u);
+    uint32_t all_or = __reduce_or_sync(0xffffffffu, lane < NW ? s_or[lane] : 0u);
+    if (C > 1) {
+        // every CTA's AND/OR to every CTA; then all keys and scores of the
+        // unit are in place (the barrier orders the stores before it,
+        // shared and global, for every thread of the cluster)
+        if (tid < C) {
+            ptx::st_cluster_u32(ptx::cluster_map(ptx::smem_u32(&c_and[rank]), (uint32_t)tid), all_and);
+            ptx::st_cluster_u32(ptx::cluster_map(ptx::smem_u32(&c_or[rank]), (uint32_t)tid), all_or);
+        }
+        ptx::cluster_sync();
+        all_and = __reduce_and_sync(0xffffffffu, lane < C ? c_and[lane] : ~0u);
+        all_or = __reduce_or_sync(0xffffffffu, lane < C ? c_or[lane] : 0u);
+    }
     const RadixScratch rs{hist, comb, gtot, rout};
     const uint32_t E = (uint32_t)(m - B);
     const Cut cut = radix_cut<NT>([&](int j, uint32_t& k) { k = vals[j]; return true; }, m, (uint32_t)m, E,
-                                  __reduce_and_sync(0xffffffffu, lane < NW ? s_and[lane] : ~0u),
-                                  __reduce_or_sync(0xffffffffu, lane < NW ? s_or[lane] : 0u), rs);
+                                  all_and, all_or, rs);
     // equal scores on both sides of the cut (every bit compared, some of the
     // boundary keys kept): of those, the lower positions are kept
     Cut tie{0u, 0u, 0u, 0u};
@@ -289,7 +332,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
         const uint32_t hb = __ballot_sync(0xffffffffu, ev && j < B);
         const uint32_t mb = __ballot_sync(0xffffffffu, !ev && j < m && j >= B);
         // surviving frame rows that stay in place get their position
-        if (!ev && j >= c && j < min(B, m)) pos[j] = a.pos_base + (j - c);
+        if (rank == 0 && !ev && j >= c && j < min(B, m)) pos[j] = a.pos_base + (j - c);
         if (lane == 0) { hmask[q] = hb; mmask[q] = mb; }
         nh += __popc(hb);
         nm += __popc(mb);
@@ -310,7 +353,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
         if (lane == 31) {
             // every hole gets a mover
             s_pairs = min(ph, pm);
-            if (ph != pm) record_error(a.err, (uint32_t)STATEKV_E_DEVICE, kSiteSelect, ph * 65536u + pm);
+            if (ph != pm && rank == 0)
+                record_error(a.err, (uint32_t)STATEKV_E_DEVICE, kSiteSelect, ph * 65536u + pm);
         }
     }
     __syncthreads();
@@ -328,7 +372,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     }
     __syncthreads();
     const uint32_t np = s_pairs;
-    for (uint32_t r = tid; r < np; r += NT) pos[holes[r]] = a.pos_base + (movers[r] - c);
+    // this CTA's pairs [p_lo, p_hi)
+    const uint32_t p_lo = (uint32_t)((uint64_t)np * rank / C);
+    const uint32_t p_hi = (uint32_t)((uint64_t)np * (rank + 1) / C);
+    for (uint32_t r = p_lo + tid; r < p_hi; r += NT) pos[holes[r]] = a.pos_base + (movers[r] - c);
 
     // ---- row moves (K and V), 16-byte vectors.  Holes are slots < B and
     // movers slots >= B, so no row is both read and written: each thread
@@ -339,8 +386,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     const int64_t unit_bytes = (int64_t)a.slots * a.row_bytes;
     uint4* pk = reinterpret_cast<uint4*>((char*)a.pool_k + u * unit_bytes);
     uint4* pv = reinterpret_cast<uint4*>((char*)a.pool_v + u * unit_bytes);
-    const int64_t total = (int64_t)np * vpr;
-    for (int64_t e0 = tid; e0 < total; e0 += MV * NT) {
+    const int64_t total = (int64_t)p_hi * vpr;
+    for (int64_t e0 = (int64_t)p_lo * vpr + tid; e0 < total; e0 += MV * NT) {
         uint4 vk[MV], vv[MV];
         int64_t dst[MV];
 #pragma unroll
@@ -371,22 +418,74 @@ size_t select_smem_bytes(int slots, int T) {
 }
 
 template <int NT>
-cudaError_t launch_select_nt(const SelectArgs& a, cudaStream_t st) {
-    // a handle that never evicts never reaches the key buffer
-    size_t smem = a.never_evicts ? 0 : select_smem_bytes(a.slots, a.T);
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<NT>,
-        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+cudaLaunchConfig_t select_config(const SelectArgs& a, cudaStream_t st, size_t smem, int C,
+                                 cudaLaunchAttribute (&attr)[2]) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.U);
+    cfg.gridDim = dim3((unsigned)(a.U * C));
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
+    return cfg;
+}
+
+// CTAs per unit: the largest C in {8, 4} for which the device holds all U
+// clusters at once (one 1024-thread CTA per SM), else 1.  Pairs (C = 2)
+// measured no faster than one CTA per unit on the 56-unit stack, whose
+// selection starts while the attention kernel's last wave still runs.
+// Cached per (device, shared memory size).
+int select_cluster_size(const SelectArgs& a, size_t smem) {
+    if (const char* e = std::getenv("STATEKV_SELECT_CLUSTER")) {
+        const int v = std::atoi(e);
+        if (v == 1 || v == 2 || v == 4 || v == 8) return v;
+    }
+    if (a.U > a.num_sms / 4) return 1;
+    static std::mutex mu;
+    struct Entry { int dev; size_t smem; int per_wave[9]; };
+    static std::vector<Entry> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry* ent = nullptr;
+    for (auto& x : cache)
+        if (x.dev == dev && x.smem == smem) ent = &x;
+    if (!ent) {
+        cache.push_back(Entry{dev, smem, {}});
+        ent = &cache.back();
+        for (int C = 4; C <= 8; C *= 2) {
+            cudaLaunchAttribute attr[2];
+            SelectArgs probe = a;
+            probe.U = 1;
+            const cudaLaunchConfig_t cfg = select_config<1024>(probe, nullptr, smem, C, attr);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, select_kernel<1024>, &cfg) != cudaSuccess) n = 0;
+            ent->per_wave[C] = n;
+        }
+        cudaGetLastError();
+    }
+    for (int C = 8; C >= 4; C /= 2)
+        if (ent->per_wave[C] >= a.U) return C;
+    return 1;
+}
+
+template <int NT>
+cudaError_t launch_select_nt(const SelectArgs& a_in, cudaStream_t st) {
+    // a handle that never evicts never reaches the key buffer
+    size_t smem = a_in.never_evicts ? 0 : select_smem_bytes(a_in.slots, a_in.T);
+    cudaError_t e = cudaFuncSetAttribute(select_kernel<NT>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    SelectArgs a = a_in;
+    a.cluster = NT == 1024 ? select_cluster_size(a, smem) : 1;
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = select_config<NT>(a, st, smem, a.cluster, attr);
     return cudaLaunchKernelEx(&cfg, select_kernel<NT>, a);
 }
 

@@ -63,10 +63,11 @@ struct AttnArgs {
     int32_t U, GT, T, d, slots, c, m_pad, n_row_tiles;
     float scale_log2;     // mscale^2/sqrt(d) * log2(e)
     float scale;          // mscale^2/sqrt(d)
-    // query tiles [split_item0, U * n_row_tiles) run as key-split CTA pairs
-    // (set by the launcher); resident = CTAs one wave holds (one per SM; 0:
-    // never split)
+    // query tiles [split_item0, U * n_row_tiles) run split over the keys,
+    // each by the split_ks CTAs of a cluster (set by the launcher); resident
+    // = CTAs one wave holds (one per SM; 0: never split)
     int32_t split_item0;
+    int32_t split_ks;
     int32_t resident;
 };
 
@@ -83,6 +84,7 @@ struct SelectArgs {
     int32_t window;       // 1: keep the B most recent tokens instead of Top-B
     int32_t never_evicts; // B >= every pool size this handle can reach
     int32_t num_sms;      // SMs of the device (sets the CTA size)
+    int32_t cluster;      // CTAs per unit (a thread-block cluster; set by the launcher)
 };
 
 cudaError_t launch_rope_table(const RopeTableArgs& a, cudaStream_t st);

@@ -399,7 +399,8 @@ class _ZeroKeys:
         return q, np.zeros_like(k), v
 
 
-def test_exact_score_ties_keep_the_lower_positions():
+@pytest.mark.parametrize("cluster", ["1", "8"])
+def test_exact_score_ties_keep_the_lower_positions(cluster, monkeypatch):
     """With K = 0 (so K' = 0 after RoPE) every logit is 0 and P is uniform
     over each query row's visible keys: every compressed key and the frame's
     key 0 (visible to every row) get bit-identical scores, the frame's later
@@ -407,7 +408,9 @@ def test_exact_score_ties_keep_the_lower_positions():
     evictions) falls inside that tied group -- keys 1..T-1 plus one of the
     tied keys -- and the tie rule (the lower position wins) keeps the
     compressed keys: C holds positions 0..B-1 for ever.  Checked exactly, with
-    no near-tie allowance."""
+    no near-tie allowance.  Run with each unit's selection on one CTA and on
+    a cluster of eight."""
+    monkeypatch.setenv("STATEKV_SELECT_CLUSTER", cluster)
     sh = _small("ties", q_heads=4, kv_heads=2, layers=2, frames=7)
     st = Stepper(sh)
     st.src = _ZeroKeys(st.src)
@@ -426,9 +429,11 @@ def test_exact_score_ties_keep_the_lower_positions():
                 np.testing.assert_array_equal(kept, np.arange(min(B, (n + 1) * T)))
 
 
-def test_window_policy_keeps_the_most_recent_tokens():
+@pytest.mark.parametrize("cluster", ["1", "4"])
+def test_window_policy_keeps_the_most_recent_tokens(cluster, monkeypatch):
     """The sliding-window baseline on the same kernels: every step checked,
     through the fill and well past it."""
+    monkeypatch.setenv("STATEKV_SELECT_CLUSTER", cluster)
     sh = _small("window", q_heads=4, kv_heads=2, head_dim=128, frame_tokens=64,
                 budget=160, frames=6)
     st = Stepper(sh, policy="window")
@@ -501,18 +506,80 @@ def test_overlapped_launches_match_serialised():
                                y.view(torch.int16) if y.dtype == torch.bfloat16 else y), f"C of layer {l}"
 
 
-@pytest.mark.parametrize("split,head_dim,q_heads,kv_heads,T,B", [
-    ("all", 128, 8, 2, 128, 256),     # every query tile as a key-split CTA pair
-    ("all", 64, 6, 2, 3, 7),          # one-tile keys: one half holds none
-    ("3", 128, 6, 2, 64, 200),        # the last three tiles split, the rest whole
+@pytest.mark.parametrize("split,ways,head_dim,q_heads,kv_heads,T,B", [
+    ("all", 2, 128, 8, 2, 128, 256),  # every query tile as a key-split CTA pair
+    ("all", 2, 64, 6, 2, 3, 7),       # one-tile keys: one half holds none
+    ("3", 2, 128, 6, 2, 64, 200),     # the last three tiles split, the rest whole
+    ("all", 3, 128, 8, 2, 128, 300),  # odd ways: owner blocks of 48 columns, the last 32
+    ("all", 4, 64, 6, 2, 64, 700),    # 16-column owner blocks
+    ("all", 5, 64, 14, 2, 64, 1000),  # 16-column blocks, the fifth CTA owns none
+    ("all", 6, 128, 12, 2, 96, 900),  # 24-column blocks spanning 32-column chunks
+    ("all", 8, 128, 4, 2, 128, 1200), # eight CTAs, 16-column blocks
+    ("all", 8, 64, 6, 2, 3, 7),       # more CTAs than key tiles: most hold none
+    ("2", 4, 128, 12, 2, 64, 200),    # 6 tiles: 4 whole (one cluster of 4), 2 split 4 ways
 ])
-def test_key_split_query_tiles(split, head_dim, q_heads, kv_heads, T, B, monkeypatch):
-    """Query tiles computed by two CTAs of a cluster, one key half each
-    (lse partials and O columns exchanged through distributed shared
+def test_key_split_query_tiles(split, ways, head_dim, q_heads, kv_heads, T, B, monkeypatch):
+    """Query tiles computed by the `ways` CTAs of a cluster, one key range
+    each (lse partials and O columns exchanged through distributed shared
     memory): every frame against the oracle."""
     monkeypatch.setenv("STATEKV_ATTN_SPLIT", split)
+    monkeypatch.setenv("STATEKV_ATTN_SPLIT_WAYS", str(ways))
     sh = _small("split", q_heads=q_heads, kv_heads=kv_heads, head_dim=head_dim,
                 frame_tokens=T, budget=B, frames=6)
     st = Stepper(sh)
     for n in range(sh.frames):
         st.step(n)
+
+
+@pytest.mark.parametrize("name", ["internvl3_2b_stack", "qwen3vl_2b_stack"])
+def test_one_layer_per_launch_steady_state(name):
+    """One layer per launch (a model whose layers feed each other): fewer
+    query tiles than SMs, so every tile's keys are spread over a cluster of
+    CTAs chosen from the device's cluster occupancy; checked on every unit
+    through the fill and at a full state."""
+    sh = SHAPES[name].with_(name=f"{name}_1layer", layers=1, frames=24)
+    st = Stepper(sh)
+    for n in range(sh.frames):
+        if n in (0, 1, 16, 17):
+            st.step(n)
+        else:
+            st.run(n)
+
+
+def test_split_launches_are_deterministic():
+    """A split launch gives the same bits on a replay (every CTA of a split
+    tile combines the partials in rank order)."""
+    sh = SHAPES["internvl3_1b_layer"].with_(frames=20)
+    st = Stepper(sh)
+    first = [st.run(n).cpu() for n in range(18)]
+    st.h.reset()
+    again = [st.run(n).cpu() for n in range(18)]
+    for x, y in zip(first, again):
+        assert raw_equal(x, y)
+
+
+@pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
+def test_select_cluster_sizes_agree(cluster, monkeypatch):
+    """A unit's selection spread over 1, 2, 4 or 8 CTAs of a cluster (each
+    finishes the scores of a slice of the candidates, the keys are shared
+    through distributed shared memory, every CTA runs the cut and moves a
+    share of the rows): every frame against the oracle, and the same scores,
+    kept positions and C contents, bit for bit, as on one CTA."""
+    sh = _small("selcl", layers=3, q_heads=4, kv_heads=2, head_dim=128, frame_tokens=64,
+                budget=160, frames=6)
+    monkeypatch.setenv("STATEKV_SELECT_CLUSTER", "1")
+    ref = Stepper(sh)
+    monkeypatch.setenv("STATEKV_SELECT_CLUSTER", cluster)
+    st = Stepper(sh)
+    for n in range(sh.frames):
+        monkeypatch.setenv("STATEKV_SELECT_CLUSTER", "1")
+        ref.run(n)
+        monkeypatch.setenv("STATEKV_SELECT_CLUSTER", cluster)
+        st.step(n)
+        for l in range(sh.layers):
+            a, b = ref.h.compressed(0, l), st.h.compressed(0, l)
+            assert a[3] == b[3]
+            for x, y in zip(a[:3], b[:3]):
+                assert raw_equal(x.cpu(), y.cpu()), f"C of layer {l}, frame {n}"
+            sa, sb = ref.h.scores(0, l), st.h.scores(0, l)
+            assert raw_equal(sa[0].cpu(), sb[0].cpu()), f"scores of layer {l}, frame {n}"
