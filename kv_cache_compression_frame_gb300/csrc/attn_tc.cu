@@ -594,10 +594,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 // partials in rank order, so every CTA gets the same bits
                 const float part = l > 0.f ? fmaf(m, sc, log2f(l)) : -INFINITY;
                 const uint32_t slot = sbase + L::OFF_XLSE + 4u * (uint32_t)(rank * 128 + row);
-                for (int j = 0; j < ks; ++j) {
-                    if (j == rank) continue;
-                    ptx::st_cluster_f32(ptx::cluster_map(slot, (uint32_t)j), part);
-                    ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XLSE), (uint32_t)j));
+                for (int j = 0; j < ks; ++j)
+                    if (j != rank) ptx::st_cluster_f32(ptx::cluster_map(slot, (uint32_t)j), part);
+                // the warp's 32 rows, then one fence and one 32-count arrive
+                // per destination
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::fence_acq_rel_cluster();
+                    for (int j = 0; j < ks; ++j)
+                        if (j != rank)
+                            ptx::mbar_arrive_remote_relaxed(
+                                ptx::cluster_map(sy.bar(L::B_XLSE), (uint32_t)j), 32u);
                 }
                 if (!sy.wait_cluster(L::B_XLSE, 0, kSiteCol)) ok = false;
                 const float* xl = reinterpret_cast<const float*>(base + L::OFF_XLSE);
@@ -699,12 +706,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         if (SPLIT && coop) {
             // this CTA's key tiles are consumed: the others may put their O
-            // columns into our K stages
+            // columns into our K stages (the signal orders no memory access:
+            // the products that read the stages completed before S_FULL)
             __syncwarp();
             if (lane == 0)
                 for (int j = 0; j < ks; ++j)
                     if (j != rank)
-                        ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XREADY), (uint32_t)j));
+                        ptx::mbar_arrive_remote_relaxed(
+                            ptx::cluster_map(sy.bar(L::B_XREADY), (uint32_t)j), 1u);
         }
         if (me.nt > 0 && (!coop || rank == ks - 1))    // the CTA holding the last tiles
             for (int kk = me.nt * L::BN + sw * 32 + lane; kk < a.m_pad; kk += 32 * L::SW)
@@ -748,9 +757,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                             }
                         }
                     }
-                    for (int o = o_lo; o <= o_hi; ++o)
-                        if (o != rank)
-                            ptx::mbar_arrive_remote(ptx::cluster_map(sy.bar(L::B_XO), (uint32_t)o));
+                    // the warp's stores, then one fence and one 32-count
+                    // arrive per owner
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::fence_acq_rel_cluster();
+                        for (int o = o_lo; o <= o_hi; ++o)
+                            if (o != rank)
+                                ptx::mbar_arrive_remote_relaxed(
+                                    ptx::cluster_map(sy.bar(L::B_XO), (uint32_t)o), 32u);
+                    }
                 }
                 const int lo = max(c0, rank * bw), hi = min(c0 + 32, (rank + 1) * bw);
                 if (lo < hi && sy.wait_cluster(L::B_XO, 0, kSiteCol) && me.row0 + row < a.GT) {

@@ -83,6 +83,20 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
                  :: "r"(cluster_addr) : "memory");
 }
+// `count` arrivals at once on another CTA's barrier, ordering nothing: for
+// signals that order no memory access, or after fence_acq_rel_cluster().
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr, uint32_t count) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0], %1;"
+                 :: "r"(cluster_addr), "r"(count) : "memory");
+}
+// Orders every write this thread performed, or observed before it (a warp's
+// stores before a __syncwarp), before its later writes, at cluster scope.
+// One fence after a warp's distributed shared memory stores, then relaxed
+// arrives, replaces a release arrive per thread and destination (each of
+// which waits for the thread's stores on its own).
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
 // Non-blocking probe of the phase with the given parity.
 __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
     uint32_t ok;
