@@ -149,7 +149,9 @@ __device__ Cut radix_cut(const KeyOf& key_of, int m, uint32_t n, uint32_t R, uin
     return q;
 }
 
-template <int NT>
+// CL: a unit may be a cluster of a.cluster CTAs (the few-unit launch); the
+// one-CTA-per-unit launch is compiled without the cluster steps.
+template <int NT, bool CL>
 __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     constexpr int NW = NT / 32;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -176,18 +178,20 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     // it writes the pool rows read here)
     // a cluster's CTAs store keys into each other's shared memory: each
     // first has to know the others have started (arrive here, wait below)
-    const bool cl_bar = a.cluster > 1 && a.c + a.T > a.B;
+    const bool cl_bar = CL && a.cluster > 1 && a.c + a.T > a.B;
     if (cl_bar) ptx::cluster_arrive_relaxed();
     ptx::dep_wait();
     ptx::dep_trigger();
-    const int C = a.cluster;
-    const int rank = C > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int C = CL ? a.cluster : 1;
+    const int rank = CL && C > 1 ? (int)ptx::cluster_ctarank() : 0;
     const int u = (int)blockIdx.x / C;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int c = a.c, T = a.T, B = a.B;
     const int m = c + T;
-    const int j_lo = rank * m / C, j_hi = (rank + 1) * m / C;   // this CTA's candidates
+    // this CTA's candidates [j_lo, j_hi): groups of 4 (16-byte aligned)
+    const int g4 = (m + 3) / 4;
+    const int j_lo = 4 * (rank * g4 / C), j_hi = min(m, 4 * ((rank + 1) * g4 / C));
     int32_t* pos = a.pos + (int64_t)u * a.slots;
     if (m > B) {                                // the histograms start at zero
         uint4* hv = reinterpret_cast<uint4*>(hist);
@@ -202,47 +206,47 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     const float* cs = a.colsum + (int64_t)u * a.n_row_tiles * a.m_pad;
     float* scores = a.scores + (int64_t)u * a.m_pad;
     int32_t* spos = a.score_pos + (int64_t)u * a.m_pad;
-    constexpr int KU = 2, TU = 12;
+    // each thread takes 4 consecutive candidates (16-byte loads of each
+    // tile's partials: the whole unit's partials are in flight at once)
+    constexpr int TU = 12;
     const int n_rt = a.n_row_tiles;
     uint32_t k_and = ~0u, k_or = 0u;
     const uint32_t vals_s = ptx::smem_u32(vals);
     if (cl_bar) ptx::cluster_wait();
-    for (int j0 = j_lo + tid; j0 < j_hi; j0 += KU * NT) {
-        float sv[KU];
-        int32_t pv[KU];
+    for (int j0 = j_lo + 4 * tid; j0 < j_hi; j0 += 4 * NT) {
+        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        int32_t pv[4];
 #pragma unroll
-        for (int q = 0; q < KU; ++q) {
-            const int j = j0 + q * NT;
-            sv[q] = 0.f;
-            pv[q] = 0;
-            if (j < j_hi) pv[q] = j < c ? pos[j] : a.pos_base + (j - c);
+        for (int e = 0; e < 4; ++e) {
+            const int j = j0 + e;
+            pv[e] = j < c ? pos[min(j, j_hi - 1)] : a.pos_base + (j - c);
         }
         for (int t0 = 0; t0 < n_rt; t0 += TU) {
-            float part[KU][TU];
+            float4 part[TU];
 #pragma unroll
-            for (int q = 0; q < KU; ++q) {
-                const int j = j0 + q * NT;
-#pragma unroll
-                for (int tt = 0; tt < TU; ++tt)
-                    part[q][tt] = (j < j_hi && t0 + tt < n_rt)
-                                      ? __ldcg(cs + (int64_t)(t0 + tt) * a.m_pad + j) : 0.f;
-            }
+            for (int tt = 0; tt < TU; ++tt)
+                part[tt] = t0 + tt < n_rt
+                               ? __ldcg(reinterpret_cast<const float4*>(cs + (int64_t)(t0 + tt) * a.m_pad + j0))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
             // tile order: s_j has the same bits whatever the tiling above
 #pragma unroll
-            for (int q = 0; q < KU; ++q)
-#pragma unroll
-                for (int tt = 0; tt < TU; ++tt)
-                    if (t0 + tt < n_rt) sv[q] += part[q][tt];
+            for (int tt = 0; tt < TU; ++tt)
+                if (t0 + tt < n_rt) {
+                    sv[0] += part[tt].x;
+                    sv[1] += part[tt].y;
+                    sv[2] += part[tt].z;
+                    sv[3] += part[tt].w;
+                }
         }
 #pragma unroll
-        for (int q = 0; q < KU; ++q) {
-            const int j = j0 + q * NT;
+        for (int e = 0; e < 4; ++e) {
+            const int j = j0 + e;
             if (j < j_hi) {
-                sv[q] *= a.inv_rows;
-                scores[j] = sv[q];
-                spos[j] = pv[q];
+                sv[e] *= a.inv_rows;
+                scores[j] = sv[e];
+                spos[j] = pv[e];
                 if (m > B) {
-                    const uint32_t k = a.window ? (uint32_t)pv[q] : __float_as_uint(sv[q]);
+                    const uint32_t k = a.window ? (uint32_t)pv[e] : __float_as_uint(sv[e]);
                     vals[j] = k;
                     k_and &= k;
                     k_or |= k;
@@ -254,15 +258,19 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
         for (int j = max(c, j_lo) + tid; j < j_hi; j += NT) pos[j] = a.pos_base + (j - c);
         return;
     }
-    // this CTA's keys to the other CTAs of the unit (each thread sends the
-    // keys it wrote itself)
-    if (C > 1)
-        for (int j = j_lo + tid; j < j_hi; j += NT) {
-            const uint32_t k = vals[j];
-            for (int r = 0; r < C; ++r)
-                if (r != rank)
-                    ptx::st_cluster_u32(ptx::cluster_map(vals_s + 4u * (uint32_t)j, (uint32_t)r), k);
-        }
+    // this CTA's keys to the other CTAs of the unit: each thread sends the
+    // keys it stored itself above (the same indexing), so no barrier is needed
+    if (CL && C > 1)
+        for (int j0 = j_lo + 4 * tid; j0 < j_hi; j0 += 4 * NT)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = j0 + e;
+                if (j >= j_hi) break;
+                const uint32_t k = vals[j];
+                for (int r = 0; r < C; ++r)
+                    if (r != rank)
+                        ptx::st_cluster_u32(ptx::cluster_map(vals_s + 4u * (uint32_t)j, (uint32_t)r), k);
+            }
 
     // ---- 3. the cut of the E smallest keys
     {
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     __syncthreads();
     uint32_t all_and = __reduce_and_sync(0xffffffffu, lane < NW ? s_and[lane] : ~0u);
     uint32_t all_or = __reduce_or_sync(0xffffffffu, lane < NW ? s_or[lane] : 0u);
-    if (C > 1) {
+    if (CL && C > 1) {
         // every CTA's AND/OR to every CTA; then all keys and scores of the
         // unit are in place (the barrier orders the stores before it,
         // shared and global, for every thread of the cluster)
@@ -465,7 +473,8 @@ int select_cluster_size(const SelectArgs& a, size_t smem) {
             probe.U = 1;
             const cudaLaunchConfig_t cfg = select_config<1024>(probe, nullptr, smem, C, attr);
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, select_kernel<1024>, &cfg) != cudaSuccess) n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, select_kernel<1024, true>, &cfg) != cudaSuccess)
+                n = 0;
             ent->per_wave[C] = n;
         }
         cudaGetLastError();
@@ -475,22 +484,28 @@ int select_cluster_size(const SelectArgs& a, size_t smem) {
     return 1;
 }
 
-template <int NT>
-cudaError_t launch_select_nt(const SelectArgs& a_in, cudaStream_t st) {
-    // a handle that never evicts never reaches the key buffer
-    size_t smem = a_in.never_evicts ? 0 : select_smem_bytes(a_in.slots, a_in.T);
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<NT>,
+template <int NT, bool CL>
+cudaError_t launch_select_nt(const SelectArgs& a, size_t smem, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel<NT, CL>,
         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    SelectArgs a = a_in;
-    a.cluster = NT == 1024 ? select_cluster_size(a, smem) : 1;
     cudaLaunchAttribute attr[2];
     const cudaLaunchConfig_t cfg = select_config<NT>(a, st, smem, a.cluster, attr);
-    return cudaLaunchKernelEx(&cfg, select_kernel<NT>, a);
+    return cudaLaunchKernelEx(&cfg, select_kernel<NT, CL>, a);
 }
 
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
-    return a.U > a.num_sms ? launch_select_nt<512>(a, st) : launch_select_nt<1024>(a, st);
+cudaError_t launch_select(const SelectArgs& a_in, cudaStream_t st) {
+    // a handle that never evicts never reaches the key buffer
+    const size_t smem = a_in.never_evicts ? 0 : select_smem_bytes(a_in.slots, a_in.T);
+    SelectArgs a = a_in;
+    a.cluster = 1;
+    if (a.U > a.num_sms) return launch_select_nt<512, false>(a, smem, st);
+    if (cudaFuncSetAttribute(select_kernel<1024, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return cudaGetLastError();
+    a.cluster = select_cluster_size(a, smem);
+    return a.cluster > 1 ? launch_select_nt<1024, true>(a, smem, st)
+                         : launch_select_nt<1024, false>(a, smem, st);
 }
 
 }  // namespace statekv

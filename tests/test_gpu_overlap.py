@@ -10,7 +10,8 @@ next pool, so the two runs may drift apart over frames; the overlap measures
 how far.  The oracle's units run in parallel in spawned worker processes
 (the oracle itself is unchanged); each worker regenerates its own inputs
 from the seeded source.  With STATEKV_OVERLAP_OUT set, the per-layer and
-per-frame table is written there as JSON.
+per-frame table is written there as JSON; STATEKV_OVERLAP_FRAMES runs a
+longer stretch than the default 40 frames.
 """
 
 from __future__ import annotations
@@ -63,6 +64,8 @@ def _oracle_unit_stream(args):
 def test_free_running_selection_overlap_per_layer(name, layers, frames):
     from kv_cache_compression_frame_gb300 import StateKV, StateKVConfig
     sh = SHAPES[name]
+    # a longer stretch for a study (the default keeps the test to a minute or two)
+    frames = min(sh.frames, int(os.environ.get("STATEKV_OVERLAP_FRAMES", frames)))
     units = [(l, hk) for l in layers for hk in range(sh.kv_heads)]
     # the pool starts before the first CUDA call of this process's workers
     ctx = mp.get_context("spawn")
