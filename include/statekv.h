@@ -40,7 +40,9 @@
  * argument checks happen before any device work, so a call rejected with
  * E_INVALID_ARG / E_UNSUPPORTED / E_CAPACITY leaves the handle unchanged.
  * E_CUDA means a CUDA call failed (the handle's device state is then
- * unspecified; destroy it).  Device-side bounded waits that give up record a
+ * unspecified; destroy it); the call clears the CUDA runtime's last-error
+ * state before returning, so a refused launch does not resurface in later
+ * calls.  Device-side bounded waits that give up record a
  * status that statekv_check_device_status() reports as E_TIMEOUT.
  */
 #ifndef STATEKV_H_

@@ -41,6 +41,14 @@ struct StaticScratch {
 StaticScratch g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
+// A failed CUDA call: clear the runtime's last-error state (a refused launch,
+// for instance, would otherwise be reported again by the next call that
+// checks it, in this library or the caller's code) and report E_CUDA.
+int cuda_fail() {
+    cudaGetLastError();
+    return STATEKV_E_CUDA;
+}
+
 // Device address of the static scratch for the current device.
 int scratch_for_device(int dev, StaticScratch** out) {
     if (dev < 0 || dev >= kMaxDevices) return STATEKV_E_UNSUPPORTED;
@@ -48,7 +56,7 @@ int scratch_for_device(int dev, StaticScratch** out) {
     StaticScratch& s = g_scratch[dev];
     if (!s.ready) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_colsum_scratch) != cudaSuccess) return STATEKV_E_CUDA;
+        if (cudaGetSymbolAddress(&p, g_colsum_scratch) != cudaSuccess) return cuda_fail();
         s.colsum = static_cast<float*>(p);
         s.ready = true;
     }
@@ -93,7 +101,7 @@ extern "C" int statekv_attend_scores_static(
         return STATEKV_E_CAPACITY;          // larger than the fixed 16 MiB scratch
 
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return STATEKV_E_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
     StaticScratch* sc = nullptr;
     int r = scratch_for_device(dev, &sc);
     if (r != STATEKV_OK) return r;
@@ -101,7 +109,7 @@ extern "C" int statekv_attend_scores_static(
     // the status word reports this call only: a failure keeps the first
     // error it finds in a zero word, so a stale one would hide it
     if (cudaMemsetAsync(status, 0, kErrWords * sizeof(uint32_t), st) != cudaSuccess)
-        return STATEKV_E_CUDA;
+        return cuda_fail();
 
     AttnArgs a{};
     a.q_rot = q_rot; a.pool_k = pool_k; a.pool_v = pool_v; a.o = o;
@@ -116,12 +124,12 @@ extern "C" int statekv_attend_scores_static(
     if (dtype == STATEKV_BF16) {
         TcMaps maps;
         if (!make_tc_maps(&maps, pool_k, pool_v, head_dim, pool_rows, units))
-            return STATEKV_E_CUDA;
+            return cuda_fail();
         e = launch_attention_tc(a, maps, st);
     } else {
         e = launch_attention_simt(a, st);
     }
-    if (e != cudaSuccess) return STATEKV_E_CUDA;
+    if (e != cudaSuccess) return cuda_fail();
     const int m = compressed + frame_tokens;
     dim3 grid((unsigned)((m + 255) / 256), (unsigned)units);
     finish_scores_kernel<<<grid, 256, 0, st>>>(sc->colsum, scores, units, (int)n_row_tiles,

@@ -46,6 +46,14 @@ struct DeviceGuard {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// A failed CUDA call: clear the runtime's last-error state (a refused launch,
+// for instance, would otherwise be reported again by the next call that
+// checks it, in this library or the caller's code) and report E_CUDA.
+int cuda_fail() {
+    cudaGetLastError();
+    return STATEKV_E_CUDA;
+}
+
 }  // namespace
 
 struct statekv_handle {
@@ -238,7 +246,7 @@ int run_front(statekv_handle* h, const void* q, const void* k, const void* v, vo
     ra.T = T; ra.d = d; ra.slots = h->slots; ra.c = cc;
     ra.det_pitch = h->det_pitch; ra.det_row0 = h->n * T;
     e = timed(h, STATEKV_KERNEL_ROPE, st, [&] { return launch_rope(ra, c.dtype, st, true); });
-    if (e != cudaSuccess) return STATEKV_E_CUDA;
+    if (e != cudaSuccess) return cuda_fail();
 
     AttnArgs aa{};
     aa.q_rot = h->q_rot; aa.pool_k = h->pool_k; aa.pool_v = h->pool_v; aa.o = o;
@@ -251,7 +259,7 @@ int run_front(statekv_handle* h, const void* q, const void* k, const void* v, vo
         return c.dtype == STATEKV_BF16 ? launch_attention_tc(aa, h->tc, st)
                                        : launch_attention_simt(aa, st);
     });
-    if (e != cudaSuccess) return STATEKV_E_CUDA;
+    if (e != cudaSuccess) return cuda_fail();
     return STATEKV_OK;
 }
 
@@ -271,7 +279,7 @@ int run_back(statekv_handle* h, cudaStream_t st) {
     sa.never_evicts = (int64_t)c.budget >= (int64_t)c.max_frames * T;
     sa.num_sms = h->num_sms;
     cudaError_t e = timed(h, STATEKV_KERNEL_SELECT, st, [&] { return launch_select(sa, st); });
-    if (e != cudaSuccess) return STATEKV_E_CUDA;
+    if (e != cudaSuccess) return cuda_fail();
 
     h->n += 1;
     return STATEKV_OK;
@@ -307,10 +315,10 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     int v = validate(cfg);
     if (v != STATEKV_OK) return v;
     int ndev = 0;
-    if (cudaGetDeviceCount(&ndev) != cudaSuccess) { cudaGetLastError(); return STATEKV_E_CUDA; }
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) return cuda_fail();
     if (cfg->device >= ndev) return STATEKV_E_INVALID_ARG;
     DeviceGuard g(cfg->device);
-    if (!g.ok) return STATEKV_E_CUDA;
+    if (!g.ok) return cuda_fail();
 
     statekv_handle* h = new (std::nothrow) statekv_handle();
     if (!h) return STATEKV_E_OOM;
@@ -358,24 +366,24 @@ int statekv_create(const statekv_config* cfg, statekv_handle** out) {
     if (!ok) { free_all(h); delete h; return STATEKV_E_OOM; }
     if (cudaMemcpy(h->omega, om.data(), sizeof(double) * om.size(), cudaMemcpyHostToDevice) !=
         cudaSuccess) {
-        free_all(h); delete h; return STATEKV_E_CUDA;
+        free_all(h); delete h; return cuda_fail();
     }
     // the rotation of every position D can hold (frames and decoded text),
     // computed once: D row r is at virtual position position_offset + r
     {
         RopeTableArgs ta{h->omega, h->cs, c.position_offset, (int32_t)h->det_pitch, d / 2,
                          c.dtype == STATEKV_BF16 ? 8 : 4};
-        if (launch_rope_table(ta, nullptr) != cudaSuccess) { free_all(h); delete h; return STATEKV_E_CUDA; }
+        if (launch_rope_table(ta, nullptr) != cudaSuccess) { free_all(h); delete h; return cuda_fail(); }
     }
     if (c.dtype == STATEKV_BF16 &&
         !make_tc_maps(&h->tc, h->pool_k, h->pool_v, d, h->slots, h->U)) {
-        free_all(h); delete h; return STATEKV_E_CUDA;
+        free_all(h); delete h; return cuda_fail();
     }
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c.device) !=
         cudaSuccess) {
-        free_all(h); delete h; return STATEKV_E_CUDA;
+        free_all(h); delete h; return cuda_fail();
     }
-    if (cudaDeviceSynchronize() != cudaSuccess) { free_all(h); delete h; return STATEKV_E_CUDA; }
+    if (cudaDeviceSynchronize() != cudaSuccess) { free_all(h); delete h; return cuda_fail(); }
     *out = h;
     return STATEKV_OK;
 }
@@ -398,7 +406,7 @@ int statekv_prefill_frame(statekv_handle* h, const void* q, const void* k, const
     if (h->text > 0) return STATEKV_E_INVALID_ARG;   // decoding has started: reset first
     if (h->n >= h->cfg.max_frames) return STATEKV_E_CAPACITY;
     DeviceGuard g(h->cfg.device);
-    if (!g.ok) return STATEKV_E_CUDA;
+    if (!g.ok) return cuda_fail();
     return run_frame(h, q, k, v, o, reinterpret_cast<cudaStream_t>(cuda_stream));
 }
 
@@ -407,16 +415,16 @@ int statekv_prefill_frame_host(statekv_handle* h, const void* q, const void* k, 
     if (!h || !q || !k || !v || !o || h->text > 0) return STATEKV_E_INVALID_ARG;
     if (h->n >= h->cfg.max_frames) return STATEKV_E_CAPACITY;
     DeviceGuard g(h->cfg.device);
-    if (!g.ok) return STATEKV_E_CUDA;
+    if (!g.ok) return cuda_fail();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
     if (cudaMemcpyAsync(h->stage_q, q, h->q_bytes(), cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(h->stage_k, k, h->kv_bytes(), cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(h->stage_v, v, h->kv_bytes(), cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return STATEKV_E_CUDA;
+        return cuda_fail();
     int r = run_frame(h, h->stage_q, h->stage_k, h->stage_v, h->stage_o, st);
     if (r != STATEKV_OK) return r;
     if (cudaMemcpyAsync(o, h->stage_o, h->q_bytes(), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return STATEKV_E_CUDA;
+        return cuda_fail();
     return STATEKV_OK;
 }
 
@@ -461,8 +469,8 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
     if (frames == 0) return STATEKV_OK;
     if (h->n + frames > h->cfg.max_frames) return STATEKV_E_CAPACITY;
     DeviceGuard g(h->cfg.device);
-    if (!g.ok) return STATEKV_E_CUDA;
-    if (!ensure_pipeline(h)) return STATEKV_E_CUDA;
+    if (!g.ok) return cuda_fail();
+    if (!ensure_pipeline(h)) return cuda_fail();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
     const size_t qb = h->q_bytes(), kvb = h->kv_bytes();
     void* sq[2] = {h->stage_q, h->stage2_q};
@@ -474,11 +482,11 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
         return j >= kCopyWays ? n : std::min(n, (n * (size_t)j / kCopyWays + 255) / 256 * 256);
     };
     auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-    if (!ok(cudaEventRecord(h->ev_entry, st))) return STATEKV_E_CUDA;
+    if (!ok(cudaEventRecord(h->ev_entry, st))) return cuda_fail();
     for (int j = 0; j < kCopyWays; ++j)
         if (!ok(cudaStreamWaitEvent(h->s_in[j], h->ev_entry, 0)) ||
             !ok(cudaStreamWaitEvent(h->s_out[j], h->ev_entry, 0)))
-            return STATEKV_E_CUDA;
+            return cuda_fail();
     auto h2d = [&](int32_t i) -> bool {
         const int sl = i & 1;
         // the frame's inputs as one byte range [0, qb + 2 kvb): q, then k, then v
@@ -503,12 +511,12 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
         }
         return true;
     };
-    if (!h2d(0)) return STATEKV_E_CUDA;
+    if (!h2d(0)) return cuda_fail();
     for (int32_t i = 0; i < frames; ++i) {
         const int sl = i & 1;
         int r = run_front(h, sq[sl], sk[sl], sv[sl], so[sl], st);
         if (r != STATEKV_OK) return r;
-        if (!ok(cudaEventRecord(h->ev_front[sl], st))) return STATEKV_E_CUDA;
+        if (!ok(cudaEventRecord(h->ev_front[sl], st))) return cuda_fail();
         char* oi = static_cast<char*>(o) + (size_t)i * qb;
         const char* ds = static_cast<const char*>(so[sl]);
         for (int j = 0; j < kCopyWays; ++j) {
@@ -517,14 +525,14 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
                 (b1 > b0 && !ok(cudaMemcpyAsync(oi + b0, ds + b0, b1 - b0, cudaMemcpyDeviceToHost,
                                                 h->s_out[j]))) ||
                 !ok(cudaEventRecord(h->ev_out[sl][j], h->s_out[j])))
-                return STATEKV_E_CUDA;
+                return cuda_fail();
         }
         if (i + 1 < frames) {
-            if (!h2d(i + 1)) return STATEKV_E_CUDA;
+            if (!h2d(i + 1)) return cuda_fail();
             // attention(i+1) rewrites the output slot of frame i-1
             for (int j = 0; j < kCopyWays; ++j)
                 if (i >= 1 && !ok(cudaStreamWaitEvent(st, h->ev_out[(i + 1) & 1][j], 0)))
-                    return STATEKV_E_CUDA;
+                    return cuda_fail();
         }
         r = run_back(h, st);
         if (r != STATEKV_OK) return r;
@@ -532,7 +540,7 @@ int statekv_prefill_frames_host(statekv_handle* h, int32_t frames, const void* q
     for (int s2 = 0; s2 < 2 && s2 < frames; ++s2)
         for (int j = 0; j < kCopyWays; ++j)
             if (!ok(cudaStreamWaitEvent(st, h->ev_out[(frames - 1 - s2) & 1][j], 0)))
-                return STATEKV_E_CUDA;
+                return cuda_fail();
     return STATEKV_OK;
 }
 
@@ -551,7 +559,7 @@ int statekv_decode(statekv_handle* h, int32_t tokens, const void* q, const void*
     const int64_t visible = h->n * c.frame_tokens + h->text;
     if (visible + tokens > h->det_pitch) return STATEKV_E_CAPACITY;
     DeviceGuard g(c.device);
-    if (!g.ok) return STATEKV_E_CUDA;
+    if (!g.ok) return cuda_fail();
     // partial-result buffers, sized once for the whole detailed state
     const int64_t items_max = (int64_t)h->U * decode_chunks(h->det_pitch);
     if (h->dec_items < items_max) {
@@ -571,16 +579,16 @@ int statekv_decode(statekv_handle* h, int32_t tokens, const void* q, const void*
     ra.rows_kv = (int64_t)h->U * tokens;
     ra.T = tokens; ra.d = c.head_dim; ra.slots = h->slots; ra.c = 0;
     ra.det_pitch = h->det_pitch; ra.det_row0 = visible;
-    if (launch_rope(ra, c.dtype, st, false) != cudaSuccess) return STATEKV_E_CUDA;
+    if (launch_rope(ra, c.dtype, st, false) != cudaSuccess) return cuda_fail();
     DecodeMaps maps;
     if (!make_decode_maps(&maps, h->q_rot, R, npad, h->det_k, h->det_v, h->det_pitch, h->U))
-        return STATEKV_E_CUDA;
+        return cuda_fail();
     DecodeArgs da{};
     da.o = o; da.part_m = h->dec_m; da.part_l = h->dec_l; da.part_o = h->dec_o; da.err = h->err;
     da.U = h->U; da.R = R; da.tok = tokens; da.chunks = decode_chunks(visible + tokens);
     da.num_sms = h->num_sms; da.visible = visible; da.keys = visible + tokens;
     da.scale_log2 = h->scale_log2;
-    if (launch_decode(da, maps, st) != cudaSuccess) return STATEKV_E_CUDA;
+    if (launch_decode(da, maps, st) != cudaSuccess) return cuda_fail();
     h->text += tokens;
     return STATEKV_OK;
 }
@@ -627,14 +635,14 @@ int statekv_check_device_status(statekv_handle* h, void* cuda_stream) {
     if (!h) return STATEKV_E_INVALID_ARG;
     DeviceGuard g(h->cfg.device);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
-    if (cudaStreamSynchronize(st) != cudaSuccess) return STATEKV_E_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_fail();
     uint32_t w[kErrWords] = {0, 0, 0, 0};
     if (cudaMemcpy(w, h->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return STATEKV_E_CUDA;
+        return cuda_fail();
     if (w[0] == 0) return STATEKV_OK;
     std::fprintf(stderr, "statekv: device status %d at site %u (block %u, extra %u)\n",
                  (int)w[0], w[1], w[2], w[3]);
-    if (cudaMemset(h->err, 0, sizeof(w)) != cudaSuccess) return STATEKV_E_CUDA;
+    if (cudaMemset(h->err, 0, sizeof(w)) != cudaSuccess) return cuda_fail();
     return (int)(int32_t)w[0];
 }
 
@@ -684,7 +692,7 @@ int statekv_set_compressed(statekv_handle* h, int32_t s, int32_t layer, const vo
                             cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
             cudaMemcpyAsync(h->pos + u * h->slots, pos + (size_t)hk * count,
                             count * sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-            return STATEKV_E_CUDA;
+            return cuda_fail();
     }
     return STATEKV_OK;
 }
@@ -710,9 +718,9 @@ int statekv_profile_read(statekv_handle* h, int32_t kernel, double* total_ms, in
     if (!h || kernel < 0 || kernel >= STATEKV_NUM_KERNELS) return STATEKV_E_INVALID_ARG;
     DeviceGuard g(h->cfg.device);
     for (auto& e : h->pending) {
-        if (cudaEventSynchronize(e.stop) != cudaSuccess) return STATEKV_E_CUDA;
+        if (cudaEventSynchronize(e.stop) != cudaSuccess) return cuda_fail();
         float ms = 0.f;
-        if (cudaEventElapsedTime(&ms, e.start, e.stop) != cudaSuccess) return STATEKV_E_CUDA;
+        if (cudaEventElapsedTime(&ms, e.start, e.stop) != cudaSuccess) return cuda_fail();
         h->prof_ms[e.kernel] += ms;
         h->prof_n[e.kernel] += 1;
         h->spare.push_back(e.start);
