@@ -415,19 +415,45 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
 // out[u][r][:] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the
 // unit's chunks c (M = max m_c); rows r < R only.
-__global__ void decode_combine_kernel(DecodeArgs a, int npad) {
+// Merge a row's per-chunk partials (m, l, O) in chunk order.  Thread d owns
+// output column d; the chunk weights exp2(m_c - max) and sums l_c are staged
+// in shared memory per block of 128 chunks, and the partial-O loads of
+// several chunks are in flight at once (the chunks' loads are independent).
+__global__ void __launch_bounds__(kDecD) decode_combine_kernel(DecodeArgs a, int npad) {
     const int u = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
     const int64_t i0 = (int64_t)u * a.chunks;
+    __shared__ float s_w[kDecD], s_l[kDecD], s_red[kDecD / 32];
     float mx = -INFINITY;
-    for (int c = 0; c < a.chunks; ++c) mx = fmaxf(mx, a.part_m[(i0 + c) * npad + r]);
+    for (int c = d; c < a.chunks; c += kDecD) mx = fmaxf(mx, a.part_m[(i0 + c) * npad + r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((d & 31) == 0) s_red[d >> 5] = mx;
+    __syncthreads();
+    mx = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kDecD / 32; ++w) mx = fmaxf(mx, s_red[w]);
     float acc = 0.f, lsum = 0.f;
-    for (int c = 0; c < a.chunks; ++c) {
-        const int64_t pr = (i0 + c) * npad + r;
-        const float m = a.part_m[pr];
-        if (m == -INFINITY) continue;
-        const float wgt = ptx::ex2_approx(m - mx);
-        lsum = fmaf(wgt, a.part_l[pr], lsum);
-        acc = fmaf(wgt, a.part_o[pr * kDecD + d], acc);
+    for (int c0 = 0; c0 < a.chunks; c0 += kDecD) {
+        const int n = min(kDecD, a.chunks - c0);
+        __syncthreads();                            // the previous block's weights are used
+        if (d < n) {
+            const int64_t pr = (i0 + c0 + d) * npad + r;
+            const float m = a.part_m[pr];
+            // a chunk with no visible key contributes nothing
+            s_w[d] = m == -INFINITY ? -1.f : ptx::ex2_approx(m - mx);
+            s_l[d] = m == -INFINITY ? 0.f : a.part_l[pr];
+        }
+        __syncthreads();
+        const float* po = a.part_o + ((i0 + c0) * npad + r) * kDecD + d;
+#pragma unroll 8
+        for (int c = 0; c < n; ++c) {
+            const float o = po[(int64_t)c * npad * kDecD];
+            const float w = s_w[c];
+            if (w >= 0.f) {
+                lsum = fmaf(w, s_l[c], lsum);
+                acc = fmaf(w, o, acc);
+            }
+        }
     }
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.o) + ((int64_t)u * a.R + r) * kDecD + d;
     *out = __float2bfloat16_rn(acc / lsum);
