@@ -78,24 +78,28 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     // waits for this grid before it touches memory
     ptx::dep_trigger();
     const int half = a.d / 2;
-    const int tpr = half / VEC;                      // threads per row
-    int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    int64_t row = gid / tpr;
-    int j = (int)(gid - row * tpr);
-    int64_t total = a.rows_q + 2 * a.rows_kv;
-    if (row >= total) return;
+    const int tpr = half / VEC;                      // threads per row (a power of two)
+    // 32-bit index arithmetic (create bounds every row count below 2^31) and
+    // a shift for tpr: 64-bit divisions by run-time values cost ~80
+    // instructions each, more than the rest of the thread's work
+    const uint32_t gid = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t row = gid >> (31 - __clz(tpr));
+    const int j = (int)(gid & (uint32_t)(tpr - 1));
+    const uint32_t rows_q = (uint32_t)a.rows_q, rows_kv = (uint32_t)a.rows_kv;
+    if (row >= rows_q + 2u * rows_kv) return;
     const int k0 = j * VEC;
 
     const E* src;
-    int64_t src_row;
+    uint32_t src_row;
     int kind;                                        // 0 = Q, 1 = K, 2 = V
-    if (row < a.rows_q) { kind = 0; src = (const E*)a.q; src_row = row; }
-    else if (row < a.rows_q + a.rows_kv) { kind = 1; src = (const E*)a.k; src_row = row - a.rows_q; }
-    else { kind = 2; src = (const E*)a.v; src_row = row - a.rows_q - a.rows_kv; }
-    const int i = (int)(src_row % a.T);              // token index in the frame
+    if (row < rows_q) { kind = 0; src = (const E*)a.q; src_row = row; }
+    else if (row < rows_q + rows_kv) { kind = 1; src = (const E*)a.k; src_row = row - rows_q; }
+    else { kind = 2; src = (const E*)a.v; src_row = row - rows_q - rows_kv; }
+    const uint32_t unit = src_row / (uint32_t)a.T;   // (stream, layer, head) of the row
+    const int i = (int)(src_row - unit * (uint32_t)a.T);   // token index in the frame
 
     float x[VEC], y[VEC];
-    const E* base = src + src_row * a.d;
+    const E* base = src + (int64_t)src_row * a.d;
     Vec<E>::load(base + k0, x);
     Vec<E>::load(base + half + k0, y);
     if (kind != 2) {
@@ -115,13 +119,12 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
     }
     uint4 lo = Vec<E>::pack(x), hi = Vec<E>::pack(y);
     if (kind == 0) {
-        E* dst = (E*)a.q_rot + src_row * a.d;
+        E* dst = (E*)a.q_rot + (int64_t)src_row * a.d;
         *reinterpret_cast<uint4*>(dst + k0) = lo;
         *reinterpret_cast<uint4*>(dst + half + k0) = hi;
         return;
     }
-    const int64_t unit = src_row / a.T;
-    E* det = (E*)(kind == 1 ? a.det_k : a.det_v) + (unit * a.det_pitch + a.det_row0 + i) * a.d;
+    E* det = (E*)(kind == 1 ? a.det_k : a.det_v) + ((int64_t)unit * a.det_pitch + a.det_row0 + i) * a.d;
     *reinterpret_cast<uint4*>(det + k0) = lo;
     *reinterpret_cast<uint4*>(det + half + k0) = hi;
     if (a.pool_k) {                                  // text tokens go to D only
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
         // kernel may start early, see launch_rope) reads the pool's frame
         // rows, which these stores replace
         ptx::dep_wait();
-        E* pool = (E*)(kind == 1 ? a.pool_k : a.pool_v) + (unit * a.slots + a.c + i) * a.d;
+        E* pool = (E*)(kind == 1 ? a.pool_k : a.pool_v) + ((int64_t)unit * a.slots + a.c + i) * a.d;
         *reinterpret_cast<uint4*>(pool + k0) = lo;
         *reinterpret_cast<uint4*>(pool + half + k0) = hi;
     }
@@ -155,7 +158,8 @@ cudaError_t launch_rope(const RopeArgs& a, int dtype, cudaStream_t st, bool earl
     int vec = dtype == STATEKV_BF16 ? 8 : 4;
     int64_t threads = (a.rows_q + 2 * a.rows_kv) * (a.d / 2 / vec);
     int64_t blocks = (threads + 255) / 256;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    // the kernel's 32-bit thread index
+    if (blocks * 256 > 0xffffffffLL) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);

@@ -390,7 +390,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
     // issues all its loads (up to 4 vectors of K and of V) before its stores,
     // one memory round trip instead of one per vector
     constexpr int MV = 4;
-    const int vpr = a.row_bytes / 16;
+    const int vpr = a.row_bytes / 16;           // 16-byte vectors per row: a power of two
+    const int vpr_shift = 31 - __clz(vpr);
     const int64_t unit_bytes = (int64_t)a.slots * a.row_bytes;
     uint4* pk = reinterpret_cast<uint4*>((char*)a.pool_k + u * unit_bytes);
     uint4* pv = reinterpret_cast<uint4*>((char*)a.pool_v + u * unit_bytes);
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(SelectArgs a) {
             const int64_t e = e0 + (int64_t)q * NT;
             dst[q] = -1;
             if (e < total) {
-                const int r = (int)(e / vpr), w = (int)(e - (int64_t)r * vpr);
+                const int r = (int)(e >> vpr_shift), w = (int)(e & (vpr - 1));
                 const int64_t src = (int64_t)movers[r] * vpr + w;
                 dst[q] = (int64_t)holes[r] * vpr + w;
                 vk[q] = pk[src];
