@@ -286,6 +286,13 @@ class StateKV:
         N.check(self._lib.statekv_profile_kernels(self._h, mask if names else 0xffffffff),
                 "statekv_profile_kernels")
 
+    def profile_mask(self, mask: int) -> None:
+        """Bracket exactly the kernels whose bit (1 << STATEKV_KERNEL_*) is set
+        in mask while profiling; 0 brackets none (launches keep their
+        overlap) without resetting the accumulated times."""
+        N.check(self._lib.statekv_profile_kernels(self._h, int(mask) & 0xffffffff),
+                "statekv_profile_kernels")
+
     def profile_read(self) -> dict:
         """{kernel name: (total device ms, launches)} since profiling started."""
         out = {}
