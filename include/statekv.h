@@ -284,8 +284,9 @@ int statekv_get_scores(statekv_handle* h, int32_t s, int32_t layer,
                        const float** scores, const int32_t** pool_pos,
                        int32_t* m, int32_t* pitch);
 
-/* Borrowed DEVICE pointer to the last step's rotated queries Q'
- * ([S][L][Hq][T][d], storage dtype). */
+/* Borrowed DEVICE pointer to the rotated queries Q' of the last frame step
+ * ([S][L][Hq][T][d], storage dtype) or, after a text decode, of the last
+ * decode step ([S][L][Hq][tokens][d]).  Valid until the next step. */
 int statekv_get_rotated_query(statekv_handle* h, const void** q_rot);
 
 /* Set the frame index n (teacher forcing / resume); 0 <= n < max_frames. */
