@@ -71,8 +71,12 @@ template <> struct Vec<float> {
     }
 };
 
+// 6 CTAs (1536 threads) per SM, 40 registers a thread: each thread has one
+// 32-byte chunk pair of inputs in flight, so occupancy sets the bytes in
+// flight (5 CTAs at 48 registers: 15.4 us on the 2B stack, 6: 14.6 us; 8 at 32
+// registers spills: 17.9 us; two chunk pairs per thread: 16.6 us)
 template <typename E>
-__global__ void __launch_bounds__(256) rope_kernel(RopeArgs a) {
+__global__ void __launch_bounds__(256, 6) rope_kernel(RopeArgs a) {
     constexpr int VEC = Vec<E>::N;
     // the attention kernel that follows may set itself up meanwhile; it
     // waits for this grid before it touches memory
