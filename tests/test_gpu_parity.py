@@ -232,7 +232,7 @@ def test_internvl3_2b_budget_16384_steady_state():
 
 
 @pytest.mark.parametrize("name,n", [("serving_T64_B1024", 17), ("serving_T64_B4096", 65),
-                                    ("serving_T256_B1024", 5)])
+                                    ("serving_T256_B1024", 5), ("serving_T256_B4096", 17)])
 def test_serving_shape_steady_state_sampled(name, n):
     """The batched-serving configuration: 16 independent streams x 4 layers x
     8 KV heads stepped together (512 units; at T = 64 one 128-row query tile
