@@ -3,8 +3,9 @@
 //
 // StateKV ("Linear Scaling Video VLMs for Long Video Understanding"),
 // 方法详解 / 整体框架 and 关键设计 1-3.  Per frame step n, on the caller's stream:
-//   rope_table -> rope (+ D append, pool insert) -> attention (+ column sums)
-//   -> select (scores, Top-B, slot-reuse gather).
+//   rope (+ D append, pool insert) -> attention (+ column sums)
+//   -> select (scores, Top-B, slot-reuse gather);
+// the cos/sin table of every position D can hold is built once, at create.
 // Device memory per unit u = (stream, layer, KV head), all allocated at
 // create:
 //   pool K/V   [U][B+T][d]      compressed slots [0, c) then the frame's rows
