@@ -336,6 +336,29 @@ def run_gpu(args, sh):
     q1 = len(steady) // 4
     flat = (statistics.median(steady[-q1:]) / statistics.median(steady[:q1])) if q1 else None
 
+    # each kernel's time per frame over a video (every launch bracketed, the
+    # times read after every frame), medians per window of frames: where the
+    # per-frame time moves, which kernel moves (untimed)
+    windows = None
+    if args.kernel_windows > 0:
+        names = ("rope", "attention", "select")
+        h.reset()
+        h.profile_kernels()
+        h.profile_enable(True)
+        prev = {k: 0.0 for k in names}
+        rows = []
+        for n in range(frames):
+            r = n % RING
+            h.prefill_frame(dq[r], dk[r], dv[r], o, stream)
+            p = h.profile_read()
+            rows.append({k: (p[k][0] - prev[k]) * 1000.0 for k in names})
+            prev = {k: p[k][0] for k in names}
+        h.profile_enable(False)
+        w = args.kernel_windows
+        windows = [{"n0": n0, **{k: round(statistics.median([x[k] for x in rows[n0:n0 + w]]), 2)
+                                 for k in names}}
+                   for n0 in range(0, frames, w)]
+
     # e2e: host buffers through the C ABI, copies inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -489,6 +512,8 @@ def run_gpu(args, sh):
                              "last_quarter_over_first_quarter": flat},
             "e2e": e2e,
             "decode": dec,
+            **({"kernel_us_per_window": {"frames_per_window": args.kernel_windows,
+                                         "windows": windows}} if windows else {}),
             # RoPE, attention and selection per frame (the RoPE table is made
             # once, at create)
             "gpu_launches": LAUNCHES_PER_FRAME * frames * args.steps,
@@ -521,6 +546,9 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-windows", type=int, default=0,
+                    help="also run one video with every frame synchronised and report each "
+                         "kernel's median device time per window of this many frames")
     ap.add_argument("--policy", default="topb", choices=["topb", "window"],
                     help="selection: Top-B by score (the method) or the B most recent tokens "
                          "(the sliding-window baseline)")

@@ -231,6 +231,24 @@ def test_internvl3_2b_budget_16384_steady_state():
         st.step(n, units=units)
 
 
+@pytest.mark.parametrize("cluster", ["", "1"])
+def test_largest_selectable_pool(cluster, monkeypatch):
+    """The largest pool the selection takes: B + T = 24,576 candidates per
+    unit (its key buffer fills the shared memory a CTA may hold), on the 2B
+    layer geometry (two layers), checked on the first two frames with a full
+    state; once with the selection spread over a cluster (the default for
+    so few units) and once with one CTA per unit."""
+    if cluster:
+        monkeypatch.setenv("STATEKV_SELECT_CLUSTER", cluster)
+    sh = SHAPES["internvl3_2b_stack"].with_(name="internvl3_2b_maxpool", layers=2,
+                                            budget=24576 - 256, frames=97)
+    st = Stepper(sh)
+    n_full = sh.budget // sh.frame_tokens
+    st.advance(n_full)
+    for n in (n_full, n_full + 1):
+        st.step(n)
+
+
 @pytest.mark.parametrize("name,n", [("serving_T64_B1024", 17), ("serving_T64_B4096", 65),
                                     ("serving_T256_B1024", 5), ("serving_T256_B4096", 17)])
 def test_serving_shape_steady_state_sampled(name, n):
