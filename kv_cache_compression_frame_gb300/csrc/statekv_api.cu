@@ -139,7 +139,7 @@ bool dalloc(statekv_handle* h, T** p, size_t bytes) {
     void* q = nullptr;
     if (bytes == 0) bytes = 16;
     if (cudaMalloc(&q, bytes) != cudaSuccess) { cudaGetLastError(); return false; }
-    if (cudaMemset(q, 0, bytes) != cudaSuccess) { cudaFree(q); return false; }
+    if (cudaMemset(q, 0, bytes) != cudaSuccess) { cudaGetLastError(); cudaFree(q); return false; }
     h->allocs.push_back(q);
     *p = reinterpret_cast<T*>(q);
     return true;
@@ -198,21 +198,33 @@ void rope_frequencies(const statekv_config& c, std::vector<double>& om, double& 
     mscale = c.rope_alpha == 1.0 ? 1.0 : 0.1 * std::log(c.rope_alpha) + 1.0;
 }
 
+// An event from the spare list or a new one; nullptr if none can be made.
 cudaEvent_t take_event(statekv_handle* h) {
     if (!h->spare.empty()) { cudaEvent_t e = h->spare.back(); h->spare.pop_back(); return e; }
     cudaEvent_t e = nullptr;
-    cudaEventCreate(&e);
+    if (cudaEventCreate(&e) != cudaSuccess) { cudaGetLastError(); return nullptr; }
     return e;
 }
 
-// Runs one launch, bracketed by events when profiling.
+// Runs one launch, bracketed by events when profiling (a launch whose events
+// cannot be made or recorded runs unbracketed and is not counted).
 template <typename F>
 cudaError_t timed(statekv_handle* h, int kernel, cudaStream_t st, F&& launch) {
     if (!h->profiling || !((h->prof_mask >> kernel) & 1u)) return launch();
     PendingEvent pe{kernel, take_event(h), take_event(h)};
-    cudaEventRecord(pe.start, st);
+    if (!pe.start || !pe.stop || cudaEventRecord(pe.start, st) != cudaSuccess) {
+        cudaGetLastError();
+        for (cudaEvent_t ev : {pe.start, pe.stop})
+            if (ev) h->spare.push_back(ev);
+        return launch();
+    }
     cudaError_t e = launch();
-    cudaEventRecord(pe.stop, st);
+    if (cudaEventRecord(pe.stop, st) != cudaSuccess) {
+        cudaGetLastError();
+        h->spare.push_back(pe.start);
+        h->spare.push_back(pe.stop);
+        return e;
+    }
     h->pending.push_back(pe);
     return e;
 }
