@@ -242,6 +242,12 @@ def run_reference(args, sh):
 
 
 # -------------------------------------------------------------------- GPU
+def decode_text_frames(args, sh) -> int:
+    """Whole frames of detailed-state rows the decode leg's text needs (its 3
+    warm-up steps and the timed ones)."""
+    return max(1, -(-(3 + args.decode_steps) * args.decode_tokens // sh.frame_tokens))
+
+
 def run_gpu(args, sh):
     import torch
     from kv_cache_compression_frame_gb300 import StateKV, StateKVConfig
@@ -258,8 +264,10 @@ def run_gpu(args, sh):
     dk = [torch.from_numpy(r[1]).to(torch.bfloat16).to(dev) for r in ring]
     dv = [torch.from_numpy(r[2]).to(torch.bfloat16).to(dev) for r in ring]
     o = torch.empty_like(dq[0])
-    # one frame of extra detailed-state rows: room for the text of the decode leg
-    h = StateKV(StateKVConfig.from_shape(sh, max_frames=frames + 1,
+    # extra detailed-state rows for the text of the decode leg (3 warm-up
+    # steps and the timed ones), in whole frames
+    text_frames = decode_text_frames(args, sh)
+    h = StateKV(StateKVConfig.from_shape(sh, max_frames=frames + text_frames,
                                          select_policy=args.policy), device=local)
     stream = torch.cuda.current_stream(dev)
 
@@ -566,7 +574,8 @@ def main():
                                  else sh.name)
     if args.budget:
         frames = args.frames or sh.frames
-        b = (frames + 1) * sh.frame_tokens if args.budget == "full" else int(args.budget)
+        b = ((frames + decode_text_frames(args, sh)) * sh.frame_tokens if args.budget == "full"
+             else int(args.budget))
         sh = dataclasses.replace(sh, budget=b)
     if args.impl == "reference":
         run_reference(args, sh)

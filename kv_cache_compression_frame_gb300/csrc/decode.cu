@@ -53,8 +53,8 @@ struct DecLayout {
     static constexpr int OFF_RED = OFF_P + 2 * P_TILE;       // float [4 warps][N]
     static constexpr int OFF_REF = OFF_RED + 4 * N * 4;      // float [N] reference (log2 units)
     static constexpr int OFF_FAC = OFF_REF + N * 4;          // float [N] rescale factors
-    static constexpr int OFF_FLAG = OFF_FAC + N * 4;         // uint32 [4]
-    static constexpr int OFF_BAR = OFF_FLAG + 16;
+    static constexpr int OFF_FLAG = OFF_FAC + N * 4;         // uint32 [2 tile parities][4 warps]
+    static constexpr int OFF_BAR = OFF_FLAG + 32;
     static constexpr int B_KV_FULL = 0;                      // [NS]
     static constexpr int B_KV_EMPTY = B_KV_FULL + NS;        // [NS]
     static constexpr int B_Q_FULL = B_KV_EMPTY + NS;         // [2]
@@ -309,10 +309,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     exceed |= x[r] > ref[r] + kRefSlack;
                 }
                 // raise the reference of every row when any score got past it
+                // (flags alternate between two sets by tile: a warp that
+                // runs ahead writes the next tile's set while the others
+                // still read this one; it cannot get two tiles ahead, as
+                // this barrier waits for every warp)
                 exceed = __any_sync(0xffffffffu, exceed);
-                if (lane == 0) flag[q4] = exceed ? 1u : 0u;
+                volatile uint32_t* fl = flag + 4 * (g & 1);
+                if (lane == 0) fl[q4] = exceed ? 1u : 0u;
                 if (!(ok = sync4())) break;
-                const bool raise = (flag[0] | flag[1] | flag[2] | flag[3]) != 0u;
+                const bool raise = (fl[0] | fl[1] | fl[2] | fl[3]) != 0u;
                 if (raise) {
 #pragma unroll
                     for (int r = 0; r < N; ++r) {
@@ -371,7 +376,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_P_FULL + pb));
-                if (!(ok = sync4())) break;            // ref[] / fac[] reused next tile
+                // no barrier here: ref[] and fac[] are rewritten only in the
+                // next tile's raise, after a barrier that every warp reaches
+                // only once it has finished this tile
             }
             if (!ok) break;
             // ---- item epilogue: row sums, then O^T (thread = head dimension)
