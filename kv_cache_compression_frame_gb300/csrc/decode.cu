@@ -25,9 +25,12 @@
 // l and O rescaled) only when a score exceeds it by more than 2^8, which
 // keeps exp2 in range without a max reduction per tile.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 2..5 softmax / epilogue (warp w owns TMEM lane quarter
-// w % 4: keys for S^T, head dimensions for O^T).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer,
+// then the softmax / epilogue warps: warp w owns TMEM lane quarter w % 4
+// (keys for S^T, head dimensions for O^T).  With N <= 16 query rows there are
+// 4 of them (192 threads); with 32 or 64 there are 8 (320 threads), two per
+// lane quarter, each taking half of the rows: a thread exponentiates N/2
+// scores of its key per tile instead of N.
 #include "pipeline.cuh"
 
 namespace statekv {
@@ -50,11 +53,17 @@ struct DecLayout {
     static constexpr int OFF_V = OFF_K + NS * KV_TILE;
     static constexpr int OFF_Q = OFF_V + NS * KV_TILE;       // [2]
     static constexpr int OFF_P = OFF_Q + 2 * Q_TILE;         // [2]
-    static constexpr int OFF_RED = OFF_P + 2 * P_TILE;       // float [4 warps][N]
+    // softmax warps: one per TMEM lane quarter, or two (each taking half of
+    // the query rows) when the rows are many (each thread exponentiates NH
+    // scores of its key per tile)
+    static constexpr int WPQ = N >= 32 ? 2 : 1;
+    static constexpr int SWARPS = 4 * WPQ;
+    static constexpr int NH = N / WPQ;                       // query rows per softmax warp
+    static constexpr int OFF_RED = OFF_P + 2 * P_TILE;       // float [4 lane quarters][N]
     static constexpr int OFF_REF = OFF_RED + 4 * N * 4;      // float [N] reference (log2 units)
     static constexpr int OFF_FAC = OFF_REF + N * 4;          // float [N] rescale factors
-    static constexpr int OFF_FLAG = OFF_FAC + N * 4;         // uint32 [2 tile parities][4 warps]
-    static constexpr int OFF_BAR = OFF_FLAG + 32;
+    static constexpr int OFF_FLAG = OFF_FAC + N * 4;         // uint32 [2 tile parities][SWARPS]
+    static constexpr int OFF_BAR = OFF_FLAG + 8 * SWARPS;
     static constexpr int B_KV_FULL = 0;                      // [NS]
     static constexpr int B_KV_EMPTY = B_KV_FULL + NS;        // [NS]
     static constexpr int B_Q_FULL = B_KV_EMPTY + NS;         // [2]
@@ -66,13 +75,13 @@ struct DecLayout {
     static constexpr int B_O_FULL = B_P_FREE + 2;            // [2]
     static constexpr int B_O_FREE = B_O_FULL + 2;            // [2]
     static constexpr int B_DRAIN = B_O_FREE + 2;
-    static constexpr int B_SYNC4 = B_DRAIN + 1;              // the 4 softmax warps
-    static constexpr int NBAR = B_SYNC4 + 1;
+    static constexpr int B_SYNC = B_DRAIN + 1;               // the softmax warps
+    static constexpr int NBAR = B_SYNC + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static constexpr uint32_t TM_S = 0, TM_O = 2 * N;        // two S^T, two O^T buffers
     static constexpr uint32_t TMEM_COLS = 4 * N < 32 ? 32 : 4 * N;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 64 + 32 * SWARPS;
 };
 
 struct Item {
@@ -120,14 +129,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::mbar_init(sy.bar(L::B_Q_FULL + b), 1);
             ptx::mbar_init(sy.bar(L::B_Q_EMPTY + b), 1);
             ptx::mbar_init(sy.bar(L::B_S_FULL + b), 1);
-            ptx::mbar_init(sy.bar(L::B_S_READ + b), 4);
-            ptx::mbar_init(sy.bar(L::B_P_FULL + b), 4);
+            ptx::mbar_init(sy.bar(L::B_S_READ + b), L::SWARPS);
+            ptx::mbar_init(sy.bar(L::B_P_FULL + b), L::SWARPS);
             ptx::mbar_init(sy.bar(L::B_P_FREE + b), 1);
             ptx::mbar_init(sy.bar(L::B_O_FULL + b), 1);
-            ptx::mbar_init(sy.bar(L::B_O_FREE + b), 4);
+            ptx::mbar_init(sy.bar(L::B_O_FREE + b), L::SWARPS);
         }
         ptx::mbar_init(sy.bar(L::B_DRAIN), 1);
-        ptx::mbar_init(sy.bar(L::B_SYNC4), 4);
+        ptx::mbar_init(sy.bar(L::B_SYNC), L::SWARPS);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -255,7 +264,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         sy.drain(L::B_DRAIN, 0);
     } else {
         // ------------------------------------------------ softmax / epilogue
-        const int q4 = warp & 3;                       // TMEM lane quarter
+        // warp w: TMEM lane quarter w % 4 (keys of S^T, head dimensions of
+        // O^T) and query rows [r0, r0 + NH)
+        constexpr int NH = L::NH;
+        const int q4 = warp & 3;
+        const int r0 = ((warp - 2) >> 2) * NH;
         const int kk = q4 * 32 + lane;                 // key of the tile / head dimension
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         float* red = reinterpret_cast<float*>(base + L::OFF_RED);
@@ -266,32 +279,39 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int visible = (int)a.visible, keys = (int)a.keys;
         int g = 0, li = 0;
         bool ok = true;
-        // barrier of the 4 softmax warps (a bounded mbarrier wait: a warp that
+        // NH consecutive TMEM columns of this warp's lane quarter
+        auto ld_cols = [&](uint32_t taddr, uint32_t (&v)[NH]) {
+            if constexpr (NH == 16) ptx::tmem_ld_32x32b_x16(taddr, v);
+            else ptx::tmem_ld_32x32b_x32(taddr, v);
+        };
+        auto st_cols = [&](uint32_t taddr, const uint32_t (&v)[NH]) {
+            if constexpr (NH == 16) ptx::tmem_st_32x32b_x16(taddr, v);
+            else ptx::tmem_st_32x32b_x32(taddr, v);
+        };
+        // barrier of the softmax warps (a bounded mbarrier wait: a warp that
         // gave up cannot leave the others blocked)
         uint32_t sync_par = 0;
-        auto sync4 = [&]() -> bool {
+        auto sync_sm = [&]() -> bool {
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_SYNC4));
-            const bool r = sy.wait(L::B_SYNC4, sync_par, kSiteCol);
+            if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_SYNC));
+            const bool r = sy.wait(L::B_SYNC, sync_par, kSiteCol);
             sync_par ^= 1u;
             return r;
         };
         for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x, ++li) {
             const Item it = item_of(a, w);
             const int ob = li & 1;
-            float l[N];
+            float l[NH];
 #pragma unroll
-            for (int r = 0; r < N; ++r) l[r] = 0.f;
+            for (int j = 0; j < NH; ++j) l[j] = 0.f;
             if (threadIdx.x - 64 < N) ref[threadIdx.x - 64] = -INFINITY;
-            if (!(ok = sync4())) break;
+            if (!(ok = sync_sm())) break;
             for (int t = 0; t < it.tiles; ++t, ++g) {
                 const int sb = g & 1, pb = g & 1;
                 if (!(ok = sy.wait(L::B_S_FULL + sb, (uint32_t)((g >> 1) & 1), kSiteSFull))) break;
                 ptx::tc_fence_after();
-                uint32_t sr[N];
-                if constexpr (N == 16) ptx::tmem_ld_32x32b_x16(tmem + L::TM_S + sb * N + lane_base, sr);
-                else if constexpr (N == 32) ptx::tmem_ld_32x32b_x32(tmem + L::TM_S + sb * N + lane_base, sr);
-                else ptx::tmem_ld_32x32b_x64(tmem + L::TM_S + sb * N + lane_base, sr);
+                uint32_t sr[NH];
+                ld_cols(tmem + L::TM_S + sb * N + r0 + lane_base, sr);
                 ptx::tmem_ld_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -300,34 +320,37 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 // to it iff j < keys and j <= visible + r % tok
                 const int key = (it.tile0 + t) * kKeyTile + kk;
                 const int kv = key - visible;          // >= 0 only among the new keys
-                float x[N];
+                float x[NH];
                 bool exceed = false;
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
+                for (int j = 0; j < NH; ++j) {
+                    const int r = r0 + j;
                     const bool vis = key < keys && (kv < 0 || r % a.tok >= kv);
-                    x[r] = vis ? __uint_as_float(sr[r]) * sc : -INFINITY;
-                    exceed |= x[r] > ref[r] + kRefSlack;
+                    x[j] = vis ? __uint_as_float(sr[j]) * sc : -INFINITY;
+                    exceed |= x[j] > ref[r] + kRefSlack;
                 }
                 // raise the reference of every row when any score got past it
-                // (flags alternate between two sets by tile: a warp that
-                // runs ahead writes the next tile's set while the others
-                // still read this one; it cannot get two tiles ahead, as
-                // this barrier waits for every warp)
+                // (flags alternate between two sets by tile: a warp that runs
+                // ahead writes the next tile's set while the others still
+                // read this one; it cannot get two tiles ahead, as this
+                // barrier waits for every warp)
                 exceed = __any_sync(0xffffffffu, exceed);
-                volatile uint32_t* fl = flag + 4 * (g & 1);
-                if (lane == 0) fl[q4] = exceed ? 1u : 0u;
-                if (!(ok = sync4())) break;
-                const bool raise = (fl[0] | fl[1] | fl[2] | fl[3]) != 0u;
-                if (raise) {
+                volatile uint32_t* fl = flag + L::SWARPS * (g & 1);
+                if (lane == 0) fl[warp - 2] = exceed ? 1u : 0u;
+                if (!(ok = sync_sm())) break;
+                uint32_t any = 0u;
 #pragma unroll
-                    for (int r = 0; r < N; ++r) {
-                        float m = x[r];
+                for (int i = 0; i < L::SWARPS; ++i) any |= fl[i];
+                if (any != 0u) {
+#pragma unroll
+                    for (int j = 0; j < NH; ++j) {
+                        float m = x[j];
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1)
                             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                        if (lane == 0) red[q4 * N + r] = m;
+                        if (lane == 0) red[q4 * N + r0 + j] = m;
                     }
-                    if (!(ok = sync4())) break;
+                    if (!(ok = sync_sm())) break;
                     if (threadIdx.x - 64 < N) {
                         const int r = threadIdx.x - 64;
                         const float m = fmaxf(fmaxf(red[r], red[N + r]), fmaxf(red[2 * N + r], red[3 * N + r]));
@@ -336,26 +359,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         fac[r] = (old == -INFINITY) ? 0.f : ptx::ex2_approx(old - nw);
                         ref[r] = nw;
                     }
-                    if (!(ok = sync4())) break;
+                    if (!(ok = sync_sm())) break;
                     // rescale l and the O^T accumulated so far in this item
 #pragma unroll
-                    for (int r = 0; r < N; ++r) l[r] *= fac[r];
+                    for (int j = 0; j < NH; ++j) l[j] *= fac[r0 + j];
                     if (t > 0) {
                         // every PV of this item issued so far has completed
                         if (!(ok = sy.wait(L::B_P_FREE + ((g - 1) & 1), (uint32_t)(((g - 1) >> 1) & 1),
                                            kSitePEmpty))) break;
                         ptx::tc_fence_after();
-                        uint32_t orr[N];
-                        const uint32_t ta = tmem + L::TM_O + ob * N + lane_base;
-                        if constexpr (N == 16) ptx::tmem_ld_32x32b_x16(ta, orr);
-                        else if constexpr (N == 32) ptx::tmem_ld_32x32b_x32(ta, orr);
-                        else ptx::tmem_ld_32x32b_x64(ta, orr);
+                        uint32_t orr[NH];
+                        const uint32_t ta = tmem + L::TM_O + ob * N + r0 + lane_base;
+                        ld_cols(ta, orr);
                         ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int r = 0; r < N; ++r) orr[r] = __float_as_uint(__uint_as_float(orr[r]) * fac[r]);
-                        if constexpr (N == 16) ptx::tmem_st_32x32b_x16(ta, orr);
-                        else if constexpr (N == 32) ptx::tmem_st_32x32b_x32(ta, orr);
-                        else ptx::tmem_st_32x32b_x64(ta, orr);
+                        for (int j = 0; j < NH; ++j)
+                            orr[j] = __float_as_uint(__uint_as_float(orr[j]) * fac[r0 + j]);
+                        st_cols(ta, orr);
                         ptx::tmem_st_wait();
                     }
                 }
@@ -364,12 +384,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     break;
                 uint8_t* pt = base + L::OFF_P + pb * L::P_TILE;
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
+                for (int j = 0; j < NH; ++j) {
                     // masked keys give 0 (a row's reference is finite once any
                     // key was visible to it)
-                    const float p = x[r] == -INFINITY ? 0.f : ptx::ex2_approx(x[r] - ref[r]);
-                    l[r] += p;
-                    *reinterpret_cast<__nv_bfloat16*>(pt + sw128_offset(r, kk, N)) = __float2bfloat16_rn(p);
+                    const float p = x[j] == -INFINITY ? 0.f : ptx::ex2_approx(x[j] - ref[r0 + j]);
+                    l[j] += p;
+                    *reinterpret_cast<__nv_bfloat16*>(pt + sw128_offset(r0 + j, kk, N)) = __float2bfloat16_rn(p);
                 }
                 // generic-proxy stores -> visible to the tensor core
                 ptx::fence_proxy_async_smem();
@@ -383,13 +403,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!ok) break;
             // ---- item epilogue: row sums, then O^T (thread = head dimension)
 #pragma unroll
-            for (int r = 0; r < N; ++r) {
-                float s = l[r];
+            for (int j = 0; j < NH; ++j) {
+                float sm = l[j];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (lane == 0) red[q4 * N + r] = s;
+                for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
+                if (lane == 0) red[q4 * N + r0 + j] = sm;
             }
-            if (!(ok = sync4())) break;
+            if (!(ok = sync_sm())) break;
             const int64_t pidx = (int64_t)w * N;      // partial rows of this item
             if (threadIdx.x - 64 < N) {
                 const int r = threadIdx.x - 64;
@@ -398,19 +418,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             if (!(ok = sy.wait(L::B_O_FULL + ob, (uint32_t)((li >> 1) & 1), kSiteOFull))) break;
             ptx::tc_fence_after();
-            uint32_t orr[N];
-            const uint32_t ta = tmem + L::TM_O + ob * N + lane_base;
-            if constexpr (N == 16) ptx::tmem_ld_32x32b_x16(ta, orr);
-            else if constexpr (N == 32) ptx::tmem_ld_32x32b_x32(ta, orr);
-            else ptx::tmem_ld_32x32b_x64(ta, orr);
+            uint32_t orr[NH];
+            ld_cols(tmem + L::TM_O + ob * N + r0 + lane_base, orr);
             ptx::tmem_ld_wait();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(sy.bar(L::B_O_FREE + ob));
             float* po = a.part_o + pidx * kDecD;
 #pragma unroll
-            for (int r = 0; r < N; ++r) po[(int64_t)r * kDecD + kk] = __uint_as_float(orr[r]);
-            if (!(ok = sync4())) break;                // ref[] / red[] reused by the next item
+            for (int j = 0; j < NH; ++j) po[(int64_t)(r0 + j) * kDecD + kk] = __uint_as_float(orr[j]);
+            if (!(ok = sync_sm())) break;              // ref[] / red[] reused by the next item
         }
     }
     __syncthreads();
