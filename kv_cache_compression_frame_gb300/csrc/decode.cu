@@ -28,9 +28,10 @@
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer,
 // then the softmax / epilogue warps: warp w owns TMEM lane quarter w % 4
 // (keys for S^T, head dimensions for O^T).  With N <= 16 query rows there are
-// 4 of them (192 threads); with 32 or 64 there are 8 (320 threads), two per
-// lane quarter, each taking half of the rows: a thread exponentiates N/2
-// scores of its key per tile instead of N.
+// 4 of them (192 threads); with 32 there are 8 (320 threads) and with 64
+// there are 16 (576 threads), two or four per lane quarter, each taking an
+// equal share of the rows: a thread exponentiates 16 scores of its key per
+// tile whatever N.
 #include "pipeline.cuh"
 
 namespace statekv {
@@ -53,10 +54,10 @@ struct DecLayout {
     static constexpr int OFF_V = OFF_K + NS * KV_TILE;
     static constexpr int OFF_Q = OFF_V + NS * KV_TILE;       // [2]
     static constexpr int OFF_P = OFF_Q + 2 * Q_TILE;         // [2]
-    // softmax warps: one per TMEM lane quarter, or two (each taking half of
-    // the query rows) when the rows are many (each thread exponentiates NH
-    // scores of its key per tile)
-    static constexpr int WPQ = N >= 32 ? 2 : 1;
+    // softmax warps per TMEM lane quarter: one, or two or four (each taking
+    // an equal share of the query rows) when the rows are many (each thread
+    // exponentiates NH scores of its key per tile)
+    static constexpr int WPQ = N >= 64 ? 4 : N >= 32 ? 2 : 1;
     static constexpr int SWARPS = 4 * WPQ;
     static constexpr int NH = N / WPQ;                       // query rows per softmax warp
     static constexpr int OFF_RED = OFF_P + 2 * P_TILE;       // float [4 lane quarters][N]
