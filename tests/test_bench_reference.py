@@ -53,3 +53,16 @@ def test_cpu_baseline_samples_consecutive_steady_frames():
         assert len(set(st.comp_pos.tolist())) == sh.budget
     cb = bench.cpu_baseline(sh, frames=2, layers=1)
     assert cb["kind"] == "oracle" and cb["value"] > 0 and "consecutive steady-state" in cb["sample"]
+
+
+def test_decode_text_rows_cover_the_decode_leg():
+    """The handle's extra detailed-state frames hold every text token the
+    decode leg writes (3 warm-up steps and the timed ones), and --budget
+    full never evicts with that many frames."""
+    sh = _tiny()
+    for steps, tokens in ((20, 1), (30, 8), (5, 16), (0, 1)):
+        args = argparse.Namespace(decode_steps=steps, decode_tokens=tokens)
+        extra = bench.decode_text_frames(args, sh)
+        assert extra >= 1
+        assert extra * sh.frame_tokens >= (3 + steps) * tokens
+        assert (extra - 1) * sh.frame_tokens < max(1, (3 + steps) * tokens)
