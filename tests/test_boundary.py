@@ -90,6 +90,41 @@ def test_null_handle_and_pointers(lib):
     assert lib.statekv_get_scores(None, 0, 0, None, None, None, None) == N.E_INVALID_ARG
     assert lib.statekv_set_compressed(None, 0, 0, None, None, None, 0, None) == N.E_INVALID_ARG
     assert lib.statekv_profile_read(None, 0, None, None) == N.E_INVALID_ARG
+    assert lib.statekv_decode(None, 1, None, None, None, None, None) == N.E_INVALID_ARG
+    assert lib.statekv_text_tokens(None) == -1
+
+
+def _static(**kw):
+    # a valid-looking request with 16-byte aligned fake pointers: every check
+    # below fires on the host, before any device work
+    a = dict(q_rot=16, pool_k=32, pool_v=48, units=2, group=2, frame_tokens=64, head_dim=128,
+             pool_rows=256, compressed=128, logit_scale=0.1, dtype=N.BF16, o=64, scores=80,
+             status=96, stream=None)
+    a.update(kw)
+    st = a["status"]
+    return (a["q_rot"], a["pool_k"], a["pool_v"], a["units"], a["group"], a["frame_tokens"],
+            a["head_dim"], a["pool_rows"], a["compressed"], a["logit_scale"], a["dtype"], a["o"],
+            C.cast(C.c_void_p(a["scores"]), C.POINTER(C.c_float)) if a["scores"] else None,
+            st, a["stream"])
+
+
+@pytest.mark.parametrize("bad,want", [
+    (dict(q_rot=None), N.E_INVALID_ARG),
+    (dict(pool_k=40), N.E_INVALID_ARG),            # not 16-byte aligned
+    (dict(scores=None), N.E_INVALID_ARG),
+    (dict(status=None), N.E_INVALID_ARG),          # status is required
+    (dict(status=98), N.E_INVALID_ARG),            # status not 4-byte aligned
+    (dict(units=0), N.E_INVALID_ARG),
+    (dict(frame_tokens=0), N.E_INVALID_ARG),       # empty frame
+    (dict(pool_rows=100), N.E_INVALID_ARG),        # pool shorter than compressed + frame
+    (dict(logit_scale=0.0), N.E_INVALID_ARG),
+    (dict(dtype=9), N.E_INVALID_ARG),
+    (dict(head_dim=96), N.E_UNSUPPORTED),
+    (dict(pool_rows=30000, compressed=29000), N.E_UNSUPPORTED),   # beyond the selection's rows
+    (dict(group=1024, frame_tokens=128), N.E_UNSUPPORTED),        # G*T > 65536
+])
+def test_static_entry_rejects_bad_requests_on_the_host(lib, bad, want):
+    assert lib.statekv_attend_scores_static(*_static(**bad)) == want
 
 
 def test_python_config_mirror_matches_shapes():
