@@ -27,11 +27,10 @@
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer,
 // then the softmax / epilogue warps: warp w owns TMEM lane quarter w % 4
-// (keys for S^T, head dimensions for O^T).  With N <= 16 query rows there are
-// 4 of them (192 threads); with 32 there are 8 (320 threads) and with 64
-// there are 16 (576 threads), two or four per lane quarter, each taking an
-// equal share of the rows: a thread exponentiates 16 scores of its key per
-// tile whatever N.
+// (keys for S^T, head dimensions for O^T).  With 16 or 32 query rows there
+// are 8 of them (320 threads) and with 64 there are 16 (576 threads), two or
+// four per lane quarter, each taking an equal share of the rows: a thread
+// exponentiates 8 or 16 scores of its key per tile.
 #include "pipeline.cuh"
 
 namespace statekv {
@@ -54,10 +53,9 @@ struct DecLayout {
     static constexpr int OFF_V = OFF_K + NS * KV_TILE;
     static constexpr int OFF_Q = OFF_V + NS * KV_TILE;       // [2]
     static constexpr int OFF_P = OFF_Q + 2 * Q_TILE;         // [2]
-    // softmax warps per TMEM lane quarter: one, or two or four (each taking
-    // an equal share of the query rows) when the rows are many (each thread
-    // exponentiates NH scores of its key per tile)
-    static constexpr int WPQ = N >= 64 ? 4 : N >= 32 ? 2 : 1;
+    // softmax warps per TMEM lane quarter, each taking an equal share of the
+    // query rows (each thread exponentiates NH scores of its key per tile)
+    static constexpr int WPQ = N >= 64 ? 4 : 2;
     static constexpr int SWARPS = 4 * WPQ;
     static constexpr int NH = N / WPQ;                       // query rows per softmax warp
     static constexpr int OFF_RED = OFF_P + 2 * P_TILE;       // float [4 lane quarters][N]
@@ -282,11 +280,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bool ok = true;
         // NH consecutive TMEM columns of this warp's lane quarter
         auto ld_cols = [&](uint32_t taddr, uint32_t (&v)[NH]) {
-            if constexpr (NH == 16) ptx::tmem_ld_32x32b_x16(taddr, v);
+            if constexpr (NH == 8) ptx::tmem_ld_32x32b_x8(taddr, v);
+            else if constexpr (NH == 16) ptx::tmem_ld_32x32b_x16(taddr, v);
             else ptx::tmem_ld_32x32b_x32(taddr, v);
         };
         auto st_cols = [&](uint32_t taddr, const uint32_t (&v)[NH]) {
-            if constexpr (NH == 16) ptx::tmem_st_32x32b_x16(taddr, v);
+            if constexpr (NH == 8) ptx::tmem_st_32x32b_x8(taddr, v);
+            else if constexpr (NH == 16) ptx::tmem_st_32x32b_x16(taddr, v);
             else ptx::tmem_st_32x32b_x32(taddr, v);
         };
         // barrier of the softmax warps (a bounded mbarrier wait: a warp that
