@@ -27,10 +27,10 @@
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer,
 // then the softmax / epilogue warps: warp w owns TMEM lane quarter w % 4
-// (keys for S^T, head dimensions for O^T).  With 16 or 32 query rows there
-// are 8 of them (320 threads) and with 64 there are 16 (576 threads), two or
-// four per lane quarter, each taking an equal share of the rows: a thread
-// exponentiates 8 or 16 scores of its key per tile.
+// (keys for S^T, head dimensions for O^T).  With 16 query rows there are 8
+// of them (320 threads), with 32 or 64 there are 16 (576 threads): two or
+// four per lane quarter, each taking an equal share of the rows, so a thread
+// exponentiates 8 scores of its key per tile (16 at N = 64).
 #include "pipeline.cuh"
 
 namespace statekv {
@@ -55,7 +55,7 @@ struct DecLayout {
     static constexpr int OFF_P = OFF_Q + 2 * Q_TILE;         // [2]
     // softmax warps per TMEM lane quarter, each taking an equal share of the
     // query rows (each thread exponentiates NH scores of its key per tile)
-    static constexpr int WPQ = N >= 64 ? 4 : 2;
+    static constexpr int WPQ = N >= 32 ? 4 : 2;
     static constexpr int SWARPS = 4 * WPQ;
     static constexpr int NH = N / WPQ;                       // query rows per softmax warp
     static constexpr int OFF_RED = OFF_P + 2 * P_TILE;       // float [4 lane quarters][N]
