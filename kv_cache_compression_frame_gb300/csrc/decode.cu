@@ -323,12 +323,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int kv = key - visible;          // >= 0 only among the new keys
                 float x[NH];
                 bool exceed = false;
+                if ((it.tile0 + t + 1) * kKeyTile <= visible) {
+                    // a tile of earlier keys only (every tile but the last one
+                    // or two): each is visible to every row
 #pragma unroll
-                for (int j = 0; j < NH; ++j) {
-                    const int r = r0 + j;
-                    const bool vis = key < keys && (kv < 0 || r % a.tok >= kv);
-                    x[j] = vis ? __uint_as_float(sr[j]) * sc : -INFINITY;
-                    exceed |= x[j] > ref[r] + kRefSlack;
+                    for (int j = 0; j < NH; ++j) {
+                        x[j] = __uint_as_float(sr[j]) * sc;
+                        exceed |= x[j] > ref[r0 + j] + kRefSlack;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NH; ++j) {
+                        const int r = r0 + j;
+                        const bool vis = key < keys && (kv < 0 || r % a.tok >= kv);
+                        x[j] = vis ? __uint_as_float(sr[j]) * sc : -INFINITY;
+                        exceed |= x[j] > ref[r] + kRefSlack;
+                    }
                 }
                 // raise the reference of every row when any score got past it
                 // (flags alternate between two sets by tile: a warp that runs
